@@ -1,0 +1,101 @@
+/*
+ * attn.h -- C ABI of the fused attention forward (online softmax) for GB300 (sm_103a).
+ *
+ * The operation is the exact attention forward
+ *
+ *     O = softmax(scale * Q K^T + mask) V,   LSE_i = ln sum_j exp(scale * q_i . k_j)  (visible j)
+ *
+ * computed block by block with the online-softmax recurrence (running max m,
+ * running denominator l, unnormalised accumulator o~, rescale by
+ * alpha = exp(m_old - m_new) when the max rises, one division o~/l at the end),
+ * never materialising the Nq x Nk score matrix.
+ * Sources: "2.2b: FlashAttention -- Online Softmax" (hf-cn0.pages.dev), sections
+ * "The Complete Online Softmax Algorithm" and "Extending to Attention";
+ * "FlashAttention math" (aicassindra.com), sections "What we must compute" and
+ * "The block-wise update, and the full algorithm"; "Tiled attention: running
+ * max softmax" (archcrux.com) for masked keys and fully masked rows.
+ *
+ * Conventions (the pages leave these open; this library fixes them):
+ *  - Layout: Q [B,H,Nq,d], K and V [B,H,Nk,d], O [B,H,Nq,d]: row-major, contiguous,
+ *    bf16.  LSE [B,H,Nq]: fp32, natural log of the sum over visible keys of
+ *    exp(scale * q . k).
+ *  - Mask: key j is visible to query i iff j < L_b (key padding; L_b = key_padding_lens[b]
+ *    clamped to [0, Nk], or Nk when key_padding_lens is NULL) and, when causal != 0,
+ *    j <= i + (Nk - Nq) (bottom-right aligned; j <= i when Nq == Nk).  Masked scores are
+ *    -inf before the block maximum is taken.
+ *  - A row with no visible key (fully masked, or Nk == 0) gets O = 0 and LSE = -inf,
+ *    never 0/0.
+ *  - d must be 64 or 128.  scale must be finite and > 0 (1/sqrt(d) is the usual value).
+ *  - All device pointers must be 16-byte aligned (TMA); the library does not check that
+ *    they are device pointers.
+ *
+ * Ownership: the caller owns every buffer.  attn_fwd allocates no device memory per
+ * call; the library keeps one small device status word per device, created on first use.
+ * Errors: every entry point returns an attn_status; no C++ exception crosses this ABI.
+ * attn_last_error() gives a message for the calling thread's last failure.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULLPTR = -1,        /* a required pointer is NULL */
+  ATTN_ERR_BAD_SHAPE = -2,      /* negative or too-large B, H, Nq, Nk */
+  ATTN_ERR_UNSUPPORTED_D = -3,  /* d not in {64, 128} */
+  ATTN_ERR_MISALIGNED = -4,     /* a pointer is not 16-byte aligned */
+  ATTN_ERR_NO_DEVICE = -5,      /* no usable sm_103 device / CUDA runtime error at setup */
+  ATTN_ERR_LAUNCH = -6,         /* kernel launch or copy failed (message in attn_last_error) */
+  ATTN_ERR_TIMEOUT = -7,        /* a bounded device-side wait ran out (see attn_status_sync) */
+  ATTN_ERR_BAD_ARG = -8         /* scale not finite or not > 0, or another bad scalar */
+} attn_status;
+
+/*
+ * attn_fwd -- enqueue the attention forward on `stream`.
+ *   Q, K, V   device bf16 inputs (layouts above).  K and V may be NULL when Nk == 0.
+ *   O         device bf16 output [B,H,Nq,d];  LSE device fp32 output [B,H,Nq].
+ *   B, H, Nq, Nk >= 0; a call with B*H*Nq == 0 does nothing and returns ATTN_OK.
+ *   d         64 or 128.     scale   multiplies q . k before the softmax.
+ *   causal    0 or nonzero (bottom-right aligned causal mask).
+ *   key_padding_lens  device int32[B] or NULL (no padding).
+ *   stream    a cudaStream_t, or NULL for the legacy default stream.
+ * Asynchronous: returns after the launch.  Argument and launch errors are returned at
+ * once; a device-side wait timeout is reported by attn_status_sync.
+ */
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                     int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, void* stream);
+
+/*
+ * attn_fwd_host -- the same operation on HOST buffers (pinned memory recommended).
+ * Copies Q, K, V (and key_padding_lens, a host int32[B] or NULL) to the device on
+ * `stream`, runs attn_fwd, copies O and LSE back and synchronises the stream before it
+ * returns.  Uses a per-device workspace that grows to the largest problem seen and is
+ * kept until attn_release_workspace(); it allocates only when a call needs more room.
+ */
+attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                          int Nq, int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
+                          void* stream);
+
+/* Free the attn_fwd_host workspace of the current device. */
+attn_status attn_release_workspace(void);
+
+/* Synchronise `stream`, then read and clear the device status word of the current
+ * device: ATTN_ERR_TIMEOUT if a kernel's bounded wait ran out since the last check. */
+attn_status attn_status_sync(void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* attn_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

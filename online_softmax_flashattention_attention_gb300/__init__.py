@@ -1,0 +1,138 @@
+"""Python binding of the fused attention forward library (``libattn.so``, C ABI in include/attn.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and streams.  There
+is no fallback: if the library is missing or a call fails, an exception is
+raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
+           "attn_version")
+
+STATUS_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_NULLPTR", -2: "ATTN_ERR_BAD_SHAPE", -3: "ATTN_ERR_UNSUPPORTED_D",
+                -4: "ATTN_ERR_MISALIGNED", -5: "ATTN_ERR_NO_DEVICE", -6: "ATTN_ERR_LAUNCH", -7: "ATTN_ERR_TIMEOUT",
+                -8: "ATTN_ERR_BAD_ARG"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library():
+    """Load libattn.so (built by ``__graft_entry__.build()``); raises if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        sig = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]
+        for name in ("attn_fwd", "attn_fwd_host"):
+            getattr(lib, name).argtypes = sig
+            getattr(lib, name).restype = i
+        lib.attn_release_workspace.argtypes = []
+        lib.attn_release_workspace.restype = i
+        lib.attn_status_sync.argtypes = [vp]
+        lib.attn_status_sync.restype = i
+        lib.attn_last_error.argtypes = []
+        lib.attn_last_error.restype = ctypes.c_char_p
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = i
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise AttnError(rc, load_library().attn_last_error().decode())
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attn_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal, lens_ptr, stream_ptr) -> int:
+    """The C call with plain integers for pointers; returns the attn_status code."""
+    lib = load_library()
+    return lib.attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, int(causal), lens_ptr,
+                        stream_ptr)
+
+
+def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding_lens=None, stream=None):
+    """O, LSE = softmax(scale * Q K^T + mask) V and its row logsumexp, on the GPU.
+
+    Q [B,H,Nq,d], K/V [B,H,Nk,d]: contiguous bf16 CUDA tensors.  O (bf16) and LSE
+    (fp32 [B,H,Nq]) are allocated when not given.  key_padding_lens: int32 CUDA
+    tensor [B] or None.  Enqueued on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if K.shape != (B, H, Nk, d) or V.shape != (B, H, Nk, d):
+        raise ValueError("K and V must be [B, H, Nk, d] with Q's B, H and d")
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
+    if O.shape != Q.shape or O.dtype != torch.bfloat16 or not O.is_contiguous():
+        raise ValueError("O must be a contiguous bf16 tensor shaped like Q")
+    if LSE.shape != (B, H, Nq) or LSE.dtype != torch.float32 or not LSE.is_contiguous():
+        raise ValueError("LSE must be a contiguous fp32 tensor [B, H, Nq]")
+    lens_ptr = None
+    if key_padding_lens is not None:
+        if key_padding_lens.dtype != torch.int32 or not key_padding_lens.is_cuda or key_padding_lens.numel() != B:
+            raise ValueError("key_padding_lens must be an int32 CUDA tensor [B]")
+        lens_ptr = key_padding_lens.data_ptr()
+    rc = attn_fwd_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d,
+                      float(scale), causal, lens_ptr, _stream_handle(stream))
+    _check(rc)
+    return O, LSE
+
+
+def attn_fwd_host(Q, K, V, O, LSE, *, scale=None, causal=False, key_padding_lens=None, stream=None):
+    """Host-buffer variant: Q/K/V/O are CPU bf16 tensors (pinned for speed), LSE CPU fp32,
+    key_padding_lens a CPU int32 tensor or None.  Blocks until O and LSE are written."""
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lens_ptr = None if key_padding_lens is None else key_padding_lens.data_ptr()
+    lib = load_library()
+    rc = lib.attn_fwd_host(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d,
+                           float(scale), int(causal), lens_ptr, _stream_handle(stream))
+    _check(rc)
+    return O, LSE
+
+
+def status_sync(stream=None):
+    """Synchronise the stream and raise AttnError if a bounded device wait ran out."""
+    _check(load_library().attn_status_sync(_stream_handle(stream)))
+
+
+def release_workspace():
+    _check(load_library().attn_release_workspace())
+
+
+def version() -> int:
+    return load_library().attn_version()

@@ -1,0 +1,252 @@
+// Host side of the C ABI declared in include/attn.h: argument checks, TMA tensor maps,
+// the launch, the device status word and the host-buffer entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
+
+thread_local char g_err[512] = "";
+
+attn_status fail(attn_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+std::mutex g_mu;
+uint32_t* g_status[kMaxDevices] = {};
+bool g_attr_set[kMaxDevices][2] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct Workspace {
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+
+attn_status get_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
+    return fail(ATTN_ERR_NO_DEVICE, "no current CUDA device");
+  return ATTN_OK;
+}
+
+attn_status setup(int dev, uint32_t** status) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(ATTN_ERR_NO_DEVICE, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (!g_status[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+      return fail(ATTN_ERR_NO_DEVICE, "cudaGetDeviceProperties failed");
+    if (prop.major != 10 || prop.minor != 3)
+      return fail(ATTN_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, prop.major,
+                  prop.minor);
+    uint32_t* s = nullptr;
+    if (cudaMalloc(&s, sizeof(uint32_t)) != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "status word alloc failed");
+    if (cudaMemset(s, 0, sizeof(uint32_t)) != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "status word init failed");
+    g_status[dev] = s;
+  }
+  *status = g_status[dev];
+  return ATTN_OK;
+}
+
+// 3-D map over a [BH, N, d] bf16 tensor: dims (d, N, BH), box (64, 128, 1), 128-byte swizzle.
+attn_status make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return ATTN_OK;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+attn_status check_args(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                       int Nk, int d, float scale) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0)
+    return fail(ATTN_ERR_BAD_SHAPE, "negative size (B=%d H=%d Nq=%d Nk=%d)", B, H, Nq, Nk);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED_D, "d=%d; supported: 64, 128", d);
+  const long long BH = static_cast<long long>(B) * H;
+  const long long tiles = BH * ((Nq + attn::kBM - 1) / attn::kBM);
+  if (BH > INT32_MAX || tiles > INT32_MAX || static_cast<long long>(Nq) * BH > INT32_MAX * 64ll)
+    return fail(ATTN_ERR_BAD_SHAPE, "problem too large (B*H=%lld)", BH);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_BAD_ARG, "scale must be finite and > 0");
+  if (BH == 0 || Nq == 0) return ATTN_OK;
+  if (!Q || !O || !LSE) return fail(ATTN_ERR_NULLPTR, "Q, O and LSE must not be NULL");
+  if (Nk > 0 && (!K || !V)) return fail(ATTN_ERR_NULLPTR, "K and V must not be NULL when Nk > 0");
+  if (misaligned(Q) || misaligned(O) || misaligned(LSE) || (Nk > 0 && (misaligned(K) || misaligned(V))))
+    return fail(ATTN_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  return ATTN_OK;
+}
+
+template <int D>
+attn_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
+                   float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status) {
+  using C = attn::FwdCfg<D>;
+  auto kernel = attn::attn_fwd_kernel<D>;
+  const int di = (D == 128) ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_attr_set[dev][di]) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+      if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+      g_attr_set[dev][di] = true;
+    }
+  }
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv, mo;
+  attn_status st;
+  if ((st = make_map(&mq, Q, BH, Nq, D)) != ATTN_OK) return st;
+  if ((st = make_map(&mo, O, BH, Nq, D)) != ATTN_OK) return st;
+  if (Nk > 0) {
+    if ((st = make_map(&mk, K, BH, Nk, D)) != ATTN_OK) return st;
+    if ((st = make_map(&mv, V, BH, Nk, D)) != ATTN_OK) return st;
+  } else {  // never read: every row is fully masked
+    mk = mq;
+    mv = mq;
+  }
+  attn::FwdParams p;
+  p.BH = BH;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.num_qtiles = (Nq + attn::kBM - 1) / attn::kBM;
+  p.causal = causal ? 1 : 0;
+  p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.lens = lens;
+  p.lse = LSE;
+  p.status = status;
+  p.timeout_ns = kDefaultTimeoutNs;
+  const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH);
+  kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
+                     int d, float scale, int causal, const int32_t* key_padding_lens, void* stream) {
+  g_err[0] = '\0';
+  attn_status st = check_args(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  int dev;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  uint32_t* status = nullptr;
+  if ((st = setup(dev, &status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128) return launch<128>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
+  return launch<64>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
+}
+
+attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                          int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, void* stream) {
+  g_err[0] = '\0';
+  attn_status st = check_args(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  int dev;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t q_bytes = BH * Nq * d * 2, kv_bytes = BH * Nk * d * 2, lse_bytes = BH * Nq * 4;
+  const size_t lens_bytes = key_padding_lens ? static_cast<size_t>(B) * 4 : 0;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t need = 2 * up(q_bytes) + 2 * up(kv_bytes) + up(lse_bytes) + up(lens_bytes);
+  Workspace& ws = g_ws[dev];
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (ws.bytes < need) {
+      if (ws.base) cudaFree(ws.base);
+      ws.base = nullptr;
+      ws.bytes = 0;
+      if (cudaMalloc(&ws.base, need) != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "workspace alloc of %zu B failed", need);
+      ws.bytes = need;
+    }
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws.base);
+  uint8_t* dQ = w;
+  uint8_t* dO = dQ + up(q_bytes);
+  uint8_t* dK = dO + up(q_bytes);
+  uint8_t* dV = dK + up(kv_bytes);
+  float* dL = reinterpret_cast<float*>(dV + up(kv_bytes));
+  int32_t* dlens = key_padding_lens ? reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(dL) + up(lse_bytes)) : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(dQ, Q, q_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && kv_bytes) e = cudaMemcpyAsync(dK, K, kv_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && kv_bytes) e = cudaMemcpyAsync(dV, V, kv_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && lens_bytes) e = cudaMemcpyAsync(dlens, key_padding_lens, lens_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "host-to-device copy: %s", cudaGetErrorString(e));
+  st = attn_fwd(dQ, kv_bytes ? dK : nullptr, kv_bytes ? dV : nullptr, dO, dL, B, H, Nq, Nk, d, scale, causal, dlens,
+                stream);
+  if (st != ATTN_OK) return st;
+  e = cudaMemcpyAsync(O, dO, q_bytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(LSE, dL, lse_bytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "device-to-host copy: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+attn_status attn_release_workspace(void) {
+  int dev;
+  attn_status st = get_device(&dev);
+  if (st != ATTN_OK) return st;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_ws[dev].base) cudaFree(g_ws[dev].base);
+  g_ws[dev] = Workspace{};
+  return ATTN_OK;
+}
+
+attn_status attn_status_sync(void* stream) {
+  g_err[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "stream sync: %s", cudaGetErrorString(e));
+  int dev;
+  attn_status st = get_device(&dev);
+  if (st != ATTN_OK) return st;
+  uint32_t* status = g_status[dev];
+  if (!status) return ATTN_OK;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(ATTN_ERR_LAUNCH, "status read failed");
+  if (v) {
+    cudaMemset(status, 0, sizeof(uint32_t));
+    return fail(ATTN_ERR_TIMEOUT, "a bounded device wait ran out (status word 0x%x)", v);
+  }
+  return ATTN_OK;
+}
+
+const char* attn_last_error(void) { return g_err; }
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

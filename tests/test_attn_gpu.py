@@ -1,0 +1,258 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by element.
+
+Small and ragged shapes are compared whole; the full-size workloads are compared on
+sampled rows that the oracle computes one by one, plus properties that hold at any
+size.  Tolerance: see tests/gpu_helpers.py.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from gpu_helpers import compare, run_cuda, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def custom(B, H, Nq, Nk, d, causal=False, seed=7, lens=None, qk=("normal", 0.0, 1.0), v=("normal", 0.0, 1.0),
+           scale=None):
+    w = dict(name="custom", B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=causal, qk=qk, v=v, seed=seed,
+             lens=None if lens is None else ("given", lens), plant=None,
+             scale=1.0 / math.sqrt(d) if scale is None else scale)
+    return gen.make_inputs(w)
+
+
+def oracle_full(x, causal=None, lens=None):
+    return oracle.attention(x["Q"], x["K"], x["V"], x["scale"], x["causal"] if causal is None else causal,
+                            x["lens"] if lens is None else lens)
+
+
+# ------------------------------------------------------------------ small, whole
+
+SHAPES = [
+    # B, H, Nq, Nk, d, causal, lens
+    (1, 2, 256, 256, 64, False, None),
+    (1, 1, 128, 128, 128, False, None),
+    (1, 1, 1, 1, 128, False, None),
+    (2, 3, 300, 300, 128, True, None),
+    (2, 2, 129, 257, 64, False, None),
+    (1, 2, 383, 200, 128, True, None),      # Nq > Nk: first rows fully masked (bottom-right causal)
+    (1, 2, 200, 383, 128, True, None),      # Nq < Nk
+    (3, 1, 260, 260, 128, False, [0, 1, 129]),
+    (2, 2, 300, 512, 64, True, [512, 127]),
+    (1, 1, 17, 1000, 128, False, None),
+    (1, 4, 640, 640, 64, True, None),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,lens", SHAPES)
+def test_parity_small_whole(B, H, Nq, Nk, d, causal, lens):
+    x = custom(B, H, Nq, Nk, d, causal, seed=B * 1000 + Nq + Nk + d, lens=lens)
+    O, LSE = run_cuda(x)
+    O_ref, LSE_ref = oracle_full(x)
+    compare(O, LSE, O_ref, LSE_ref)
+
+
+def test_parity_workload_b1h2n256d64():
+    x = gen.make_inputs("b1h2n256d64")
+    O, LSE = run_cuda(x)
+    O_ref, LSE_ref = oracle_full(x)
+    compare(O, LSE, O_ref, LSE_ref)
+
+
+def test_nk_zero_every_row_fully_masked():
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    Q = torch.randn(1, 2, 130, 64, device="cuda").to(torch.bfloat16)
+    K = torch.empty(1, 2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    O = torch.full_like(Q, float("nan"))
+    LSE = torch.full((1, 2, 130), float("nan"), device="cuda")
+    pkg.attn_fwd(Q, K, K, O, LSE, scale=0.125)
+    pkg.status_sync()
+    assert torch.all(O == 0) and torch.all(torch.isneginf(LSE))
+
+
+# ------------------------------------------------------------------ pages' examples through the ABI
+
+def page_problem(scores, values, d=64, scale=1.0):
+    """B = H = Nq = 1: q = e0, k_j = s_j e0 (exact in bf16), v_j padded with zeros."""
+    Nk = len(scores)
+    q = np.zeros((1, 1, 1, d), np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, 1, Nk, d), np.float32)
+    k[0, 0, :, 0] = scores
+    v = np.zeros((1, 1, Nk, d), np.float32)
+    vals = np.asarray(values, np.float32).reshape(Nk, -1)
+    v[0, 0, :, :vals.shape[1]] = vals
+    return dict(Q=gen.f32_to_codes(q), K=gen.f32_to_codes(k), V=gen.f32_to_codes(v), lens=None, scale=scale,
+                causal=False)
+
+
+def test_page_example_scalar_values(golden):
+    g = golden["scalar_values"]
+    # values / 10 keep the bf16 output ulp small; o = 36.88 / 10
+    x = page_problem(g["scores"], np.array(g["v"]) / 10.0)
+    O, LSE = run_cuda(x)
+    assert abs(O[0, 0, 0, 0] * 10 - g["o"]) <= 0.08   # bf16 half-ulp of 3.688 is 0.0078, x10
+    m, l = oracle.softmax_stats(g["scores"])
+    assert abs(LSE[0, 0, 0] - (m + math.log(g["l"]))) <= 1e-3
+
+
+@pytest.mark.parametrize("key", ["attention_no_rescale", "attention_rescale"])
+def test_page_examples_two_blocks(golden, key):
+    g = golden[key]
+    x = page_problem(g["scores"], g["V"])
+    O, _ = run_cuda(x)
+    assert np.allclose(O[0, 0, 0, :2], g["output_verification"] if "output_verification" in g else g["output"],
+                       atol=5e-3)
+    # V = identity returns the probabilities themselves
+    xe = page_problem(g["scores"], np.eye(4))
+    Oe, _ = run_cuda(xe)
+    assert np.allclose(Oe[0, 0, 0, :4], g["P"], atol=2e-3)
+
+
+def test_softmax_2413_rows_through_abi(golden):
+    g = golden["softmax_2413"]
+    x = page_problem(g["scores"], np.eye(4))
+    O, LSE = run_cuda(x)
+    assert np.allclose(O[0, 0, 0, :4], g["softmax"], atol=1e-3)
+    assert abs(LSE[0, 0, 0] - math.log(np.exp(np.array(g["scores"], float)).sum())) < 1e-3
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_v_ones_rows_sum_to_one():
+    x = custom(2, 2, 300, 300, 128, True, seed=3)
+    ones = np.full_like(x["V"], gen.f32_to_codes(np.float32(1.0)))
+    x["V"] = ones
+    O, _ = run_cuda(x)
+    assert np.all(np.abs(O - 1.0) <= 2 ** -8)
+
+
+def test_padding_equals_truncation_bitwise():
+    x = custom(1, 2, 256, 700, 128, False, seed=5)
+    for L in (1, 127, 128, 129, 400, 700):
+        O, LSE = run_cuda(x, lens=[L])
+        xt = dict(x, K=np.ascontiguousarray(x["K"][:, :, :L]), V=np.ascontiguousarray(x["V"][:, :, :L]), lens=None)
+        Ot, LSEt = run_cuda(xt)
+        assert np.array_equal(O, Ot) and np.array_equal(LSE, LSEt), L
+
+
+def test_masked_key_leakage():
+    x = custom(1, 1, 128, 512, 128, False, seed=11)
+    L = 300
+    O_ref, LSE_ref = run_cuda(x, lens=[L])
+    # masked keys get a score of about +80 for query 0 (and large ones elsewhere) and
+    # values of 1e4: with the mask applied before the max nothing may move
+    K = gen.codes_to_f32(x["K"]).copy()
+    V = gen.codes_to_f32(x["V"]).copy()
+    q0 = gen.codes_to_f32(x["Q"])[0, 0, 0].astype(np.float64)
+    K[0, 0, L:] = (q0 * (80.0 / x["scale"]) / (q0 @ q0)).astype(np.float32)
+    V[0, 0, L:] = 1e4
+    x2 = dict(x, K=gen.f32_to_codes(K), V=gen.f32_to_codes(V))
+    O, LSE = run_cuda(x2, lens=[L])
+    assert np.array_equal(O, O_ref) and np.array_equal(LSE, LSE_ref)
+
+
+def test_huge_scores_stay_finite():
+    x = custom(1, 2, 256, 256, 128, False, seed=13, qk=("normal", 0.0, 16.0))
+    O, LSE = run_cuda(x)
+    O_ref, LSE_ref = oracle_full(x)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(LSE))
+    s = x["scale"] * (oracle.bf16_to_f64(x["Q"][0, 0]) @ oracle.bf16_to_f64(x["K"][0, 0]).T)
+    assert s.max() > 700  # naive exp overflows here in float64
+    err = np.abs(O - O_ref)
+    assert err.max() <= 2e-2 + 0.0 and np.abs(LSE - LSE_ref).max() <= 1e-3 * max(1.0, np.abs(LSE_ref).max() / 100)
+
+
+def test_max_in_first_vs_last_tile():
+    """One planted large score per row, in the first key tile for one run and in the
+    last for another; both must match the oracle."""
+    base = custom(1, 1, 128, 1024, 128, False, seed=17)
+    K = gen.codes_to_f32(base["K"]).astype(np.float64)
+    Q = gen.codes_to_f32(base["Q"]).astype(np.float64)
+    errs = {}
+    for where, j in (("first", 5), ("last", 1020)):
+        Qp = Q.copy()
+        k = K[0, 0, j]
+        beta = (40.0 / base["scale"] - Qp[0, 0] @ k) / (k @ k)
+        Qp[0, 0] += beta[:, None] * k
+        x = dict(base, Q=gen.f32_to_codes(Qp.astype(np.float32)))
+        O, LSE = run_cuda(x)
+        O_ref, LSE_ref = oracle_full(x)
+        errs[where] = compare(O, LSE, O_ref, LSE_ref)
+    assert errs["first"]["max_abs_o"] < 1e-2 and errs["last"]["max_abs_o"] < 1e-2
+
+
+def test_key_permutation_invariance():
+    x = custom(1, 2, 256, 384, 64, False, seed=19)
+    perm = np.random.default_rng(0).permutation(384)
+    xp = dict(x, K=np.ascontiguousarray(x["K"][:, :, perm]), V=np.ascontiguousarray(x["V"][:, :, perm]))
+    O, LSE = run_cuda(x)
+    Op, LSEp = run_cuda(xp)
+    assert np.abs(O - Op).max() <= 1e-2 and np.abs(LSE - LSEp).max() <= 1e-4
+
+
+def test_host_buffer_entry_point():
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    x = custom(2, 2, 300, 300, 128, True, seed=23, lens=[300, 150])
+    Qh, Kh, Vh = (torch.from_numpy(x[t].view(np.int16)).view(torch.bfloat16).pin_memory() for t in ("Q", "K", "V"))
+    Oh = torch.empty_like(Qh).pin_memory()
+    Lh = torch.empty((2, 2, 300), dtype=torch.float32).pin_memory()
+    pkg.attn_fwd_host(Qh, Kh, Vh, Oh, Lh, scale=x["scale"], causal=True,
+                      key_padding_lens=torch.tensor([300, 150], dtype=torch.int32))
+    O_dev, LSE_dev = run_cuda(x)
+    assert np.array_equal(Oh.float().numpy(), O_dev) and np.array_equal(Lh.numpy(), LSE_dev)
+
+
+def test_canary_guard_bands_untouched():
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    x = custom(1, 2, 200, 200, 128, True, seed=29)
+    Q, K, V = to_device(x["Q"]), to_device(x["K"]), to_device(x["V"])
+    n_o, n_l, guard = Q.numel(), 2 * 200, 4096
+    Obuf = torch.full((n_o + 2 * guard,), 7.0, device="cuda", dtype=torch.bfloat16)
+    Lbuf = torch.full((n_l + 2 * guard,), 7.0, device="cuda", dtype=torch.float32)
+    O = Obuf[guard:guard + n_o].view(Q.shape)
+    L = Lbuf[guard:guard + n_l].view(1, 2, 200)
+    pkg.attn_fwd(Q, K, V, O, L, scale=x["scale"], causal=True)
+    pkg.status_sync()
+    assert torch.all(Obuf[:guard] == 7.0) and torch.all(Obuf[guard + n_o:] == 7.0)
+    assert torch.all(Lbuf[:guard] == 7.0) and torch.all(Lbuf[guard + n_l:] == 7.0)
+
+
+def test_repeated_calls_deterministic():
+    x = custom(2, 4, 512, 512, 128, True, seed=31)
+    O1, L1 = run_cuda(x)
+    O2, L2 = run_cuda(x)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled rows
+
+FULL = ["causal_b4h16n2048d128", "causal_b2h32n8192d128", "padded_planted_b2h8n4096d128",
+        "causal_b1h32n32768d128", "causal_b1h32n32768d64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_parity_full_size_sampled(name):
+    x = gen.make_inputs(name)
+    O, LSE = run_cuda(x)
+    B, H, Nq = x["B"], x["H"], x["Nq"]
+    picks = sample_rows(B, H, Nq, n_random=40, seed=hash(name) % 1000)
+    if x["lens"] is not None:  # include rows of the fully masked batch and of the padded one
+        picks += [(0, 3, 10), (0, H - 1, Nq - 1), (1, 2, 2), (1, 5, 3)]
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], x["causal"], x["lens"], picks)
+    idx = tuple(np.array(picks).T)
+    s_v = 100.0 if x["name"].startswith("padded") else 1.0
+    compare(O[idx], LSE[idx], O_ref, LSE_ref, s_v=s_v)
+    # properties that hold everywhere: finite, fully masked batch exact
+    assert np.all(np.isfinite(O))
+    if x["lens"] is not None:
+        assert np.all(O[0] == 0) and np.all(np.isneginf(LSE[0]))
+        assert np.all(np.isfinite(LSE[1]))
+    else:
+        assert np.all(np.isfinite(LSE))
