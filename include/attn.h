@@ -94,6 +94,39 @@ const char* attn_last_error(void);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int attn_version(void);
 
+/*
+ * attn_fwd_noalloc -- attn_fwd for callers that must not allocate device memory.
+ * (An addition of this library; the source pages have no counterpart.)
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits -- a process whose device
+ * memory is handed out by someone else's pool or a fixed budget, a real-time or
+ * embedded caller that may not allocate after start-up, or a plugin that must not
+ * grow the host application's footprint.  attn_fwd itself allocates a 4-byte status
+ * word with cudaMalloc on its first call on each device; this entry point never does.
+ *
+ * Same arguments and semantics as attn_fwd, plus check_status.  The caller still
+ * passes every input and output buffer.  The only device scratch the kernel needs
+ * (one 32-bit status word for its bounded waits) lives in a fixed array compiled into
+ * the library: 256 bytes per device, held by every GPU that loads the library until
+ * the process exits.  A call whose scratch need exceeds that size is rejected with
+ * ATTN_ERR_BAD_SHAPE (the forward kernel needs 4 bytes, so today no call is).
+ *
+ *  - The first call on a device does one-time set-up with that device current: it
+ *    looks up the array's device address (cudaGetSymbolAddress) and sets the kernel
+ *    attributes.  Make that first call before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents: each call
+ *    clears the status word on `stream` before its launch.  Calls that overlap on the
+ *    GPU (different streams, or several host threads) race on that word, so their
+ *    timeout reports can be lost or misattributed; serialise them if you rely on it.
+ *  - check_status == 0: asynchronous, like attn_fwd; a device-side wait that runs out
+ *    still ends the kernel, but is not reported.  check_status != 0: the call
+ *    synchronises `stream` and returns ATTN_ERR_TIMEOUT if a wait ran out.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+attn_status attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                             int Nq, int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
+                             int check_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn.so")
 
 EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
-           "attn_version")
+           "attn_version", "attn_fwd_noalloc")
 
 STATUS_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_NULLPTR", -2: "ATTN_ERR_BAD_SHAPE", -3: "ATTN_ERR_UNSUPPORTED_D",
                 -4: "ATTN_ERR_MISALIGNED", -5: "ATTN_ERR_NO_DEVICE", -6: "ATTN_ERR_LAUNCH", -7: "ATTN_ERR_TIMEOUT",

@@ -250,3 +250,76 @@ const char* attn_last_error(void) { return g_err; }
 int attn_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free entry point.  Its device scratch is this fixed array: word 0 is the
+// status word of the kernel's bounded waits.  Host code only ever uses the array's name
+// through cudaGetSymbolAddress; the address it returns (per device) goes to the kernel.
+
+namespace {
+
+constexpr int kNoAllocScratchWords = 64;
+constexpr size_t kNoAllocScratchBytes = kNoAllocScratchWords * sizeof(uint32_t);  // 256 B per device
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+uint32_t* g_noalloc_addr[kMaxDevices] = {};
+
+// One-time set-up per device (that device current): kernel-facing address of the array,
+// device check and the tensor-map encoder.  No allocation.
+attn_status noalloc_setup(int dev, uint32_t** addr) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(ATTN_ERR_NO_DEVICE, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (!g_noalloc_addr[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+      return fail(ATTN_ERR_NO_DEVICE, "cudaGetDeviceProperties failed");
+    if (prop.major != 10 || prop.minor != 3)
+      return fail(ATTN_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, prop.major,
+                  prop.minor);
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(ATTN_ERR_NO_DEVICE, "cudaGetSymbolAddress of the scratch array failed: %s", cudaGetErrorString(e));
+    g_noalloc_addr[dev] = static_cast<uint32_t*>(p);
+  }
+  *addr = g_noalloc_addr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" attn_status attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                                        int H, int Nq, int Nk, int d, float scale, int causal,
+                                        const int32_t* key_padding_lens, int check_status, void* stream) {
+  g_err[0] = '\0';
+  attn_status st = check_args(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  const size_t need = sizeof(uint32_t);  // the forward kernel's only scratch: its status word
+  if (need > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_BAD_SHAPE, "needs %zu B of scratch; the fixed array holds %zu B", need,
+                kNoAllocScratchBytes);
+  int dev;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  uint32_t* scratch = nullptr;
+  if ((st = noalloc_setup(dev, &scratch)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, need, s);  // the array keeps the previous call's word
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
+  st = (d == 128) ? launch<128>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch)
+                  : launch<64>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch);
+  if (st != ATTN_OK || !check_status) return st;
+  uint32_t word = 0;
+  e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "reading the status word: %s", cudaGetErrorString(e));
+  if (word) return fail(ATTN_ERR_TIMEOUT, "a bounded device wait ran out (status word 0x%x)", word);
+  return ATTN_OK;
+}
