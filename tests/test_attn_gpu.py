@@ -123,6 +123,24 @@ def test_softmax_2413_rows_through_abi(golden):
 
 # ------------------------------------------------------------------ invariants
 
+def test_single_visible_key_returns_its_value_exactly():
+    """With one visible key the row max is that key's score, p = exp2(0) = 1 exactly in
+    bf16 and l = 1, so O must equal the key's value bit for bit and LSE its score.
+    A reference point above the true max (a wrong block max) still gives the right
+    LSE but breaks this exactness."""
+    for d in (64, 128):
+        x = custom(2, 2, 256, 300, d, False, seed=37 + d, lens=[1, 1])
+        O, LSE = run_cuda(x)
+        V = oracle.bf16_to_f64(x["V"])
+        assert np.array_equal(O, np.broadcast_to(V[:, :, :1, :], O.shape))
+        s0 = x["scale"] * np.einsum("bhid,bhd->bhi", oracle.bf16_to_f64(x["Q"]), oracle.bf16_to_f64(x["K"][:, :, 0]))
+        assert np.abs(LSE - s0).max() < 1e-5
+    # causal with Nq = Nk: row 0 sees key 0 only
+    x = custom(1, 2, 384, 384, 128, True, seed=43)
+    O, _ = run_cuda(x)
+    assert np.array_equal(O[:, :, 0], oracle.bf16_to_f64(x["V"])[:, :, 0])
+
+
 def test_v_ones_rows_sum_to_one():
     x = custom(2, 2, 300, 300, 128, True, seed=3)
     ones = np.full_like(x["V"], gen.f32_to_codes(np.float32(1.0)))
