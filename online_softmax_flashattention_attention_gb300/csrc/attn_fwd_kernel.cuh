@@ -47,12 +47,12 @@ constexpr uint32_t kTmemCols = 512;
 // Register split.  The CTA is launched with kLaunchRegs per thread (384 x 168 = 64512, the
 // most three warps per scheduler partition allow); the MMA/producer warpgroup then gives
 // registers back and the two softmax warpgroups take them:
-// 2 x 128 x 224 + 128 x 56 = 64512.  The host refuses to launch a build whose register
+// 2 x 128 x 208 + 128 x 88 = 64512.  The host refuses to launch a build whose register
 // count differs from kLaunchRegs, since setmaxnreg.inc would then wait for registers
 // that never come free.
 constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 224;
-constexpr int kOtherRegs = 56;
+constexpr int kSoftmaxRegs = 208;
+constexpr int kOtherRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 
 struct FwdParams {
@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = __ldg(p.lens + b);
     kv_len = L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
   }
+  // per tile: number of key blocks with a visible key, and the key limit of its first row
   int nb[kTiles], min_limit[kTiles];
   bool has_rows[kTiles];
 #pragma unroll
@@ -195,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && nblk > 0) {
         const uint64_t pol_kv = policy_evict_last();
         const uint64_t pol_q = policy_evict_first();
+#pragma unroll
         for (int t = 0; t < kTiles; ++t) {
           if (nb[t] == 0) continue;
           mbar_arrive_expect_tx(bar_q_full(t), C::kTileBytes);
@@ -229,52 +231,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
       // ============================================================== MMA issuer
       if (lane == 0 && nblk > 0) {
+        // Shared-memory descriptors: the high word (stride 1024 B, version 1, 128-byte
+        // swizzle) is the same for every operand; the low word holds the start address
+        // (>> 4) and the leading byte offset, so a k-step is one add to the low word.
+        const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
+        const uint32_t qlo0 = (sQ(0) >> 4) | (1u << 16);
+        const uint32_t qlo1 = (sQ(1) >> 4) | (1u << 16);
+        const uint32_t klo = (sK >> 4) | (1u << 16);
+        const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
+        const uint32_t ts0 = tmem + C::col_s(0), ts1 = tmem + C::col_s(1);
+        const uint32_t to0 = tmem + C::col_o(0), to1 = tmem + C::col_o(1);
+        const int nb0 = nb[0], nb1 = nb[1];
+        // S_t = Q_t K_j^T: 8 (d = 128) or 4 (d = 64) k-steps of 16
         auto issue_s = [&](int t, int j) {
-          const uint32_t kbase = sK + (j % C::kStages) * C::kTileBytes;
+          const uint32_t alo = t ? qlo1 : qlo0;
+          const uint32_t blo = klo + (j % C::kStages) * (C::kTileBytes >> 4);
+          const uint32_t d = t ? ts1 : ts0;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks / 4) * C::kSubBytes + (ks % 4) * 32;
-            mma_ss(tmem + C::col_s(t), smem_desc_sw128(sQ(t) + off, 16, 1024),
-                   smem_desc_sw128(kbase + off, 16, 1024), C::kIdescS, ks > 0 ? 1u : 0u);
+            const uint32_t off = (ks / 4) * (C::kSubBytes >> 4) + (ks % 4) * 2;
+            mma_ss(d, (static_cast<uint64_t>(dhi) << 32) | (alo + off), (static_cast<uint64_t>(dhi) << 32) | (blo + off),
+                   C::kIdescS, ks > 0 ? 1u : 0u);
           }
           mma_commit(bar_s_full(t));
         };
+        // o~_t += P_t V_j: 8 k-steps of 16 keys; A = P_t from tensor memory, B = V_j MN-major
         auto issue_pv = [&](int t, int j) {
-          const uint32_t vbase = sV + (j % C::kStages) * C::kTileBytes;
+          const uint32_t blo = vlo + (j % C::kStages) * (C::kTileBytes >> 4);
+          const uint32_t a = t ? ts1 : ts0;
+          const uint32_t d = t ? to1 : to0;
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + ks * 8,
-                   smem_desc_sw128(vbase + ks * 16 * 128, C::kSubBytes, 1024), C::kIdescO,
+            mma_ts(d, a + ks * 8, (static_cast<uint64_t>(dhi) << 32) | (blo + ks * (16 * 128 >> 4)), C::kIdescO,
                    (j > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar_pv_done(t));
         };
         bool ok = mbar_wait(bar_k_full(0), 0, wc, 3);
-        for (int t = 0; ok && t < kTiles; ++t) {
-          if (nb[t] == 0) continue;
-          ok = mbar_wait(bar_q_full(t), 0, wc, 4);
-          if (!ok) break;
+        if (ok && nb0 > 0) {
+          ok = mbar_wait(bar_q_full(0), 0, wc, 4);
           tc_fence_after();
-          issue_s(t, 0);
+          if (ok) issue_s(0, 0);
+        }
+        if (ok && nb1 > 0) {
+          ok = mbar_wait(bar_q_full(1), 0, wc, 4);
+          tc_fence_after();
+          if (ok) issue_s(1, 0);
         }
         if (ok) mma_commit(bar_k_empty(0));
         for (int j = 0; ok && j < nblk; ++j) {
           const int st = j % C::kStages;
           ok = mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 5);
           bool k_next = false;
-          for (int t = 0; ok && t < kTiles; ++t) {
-            if (j >= nb[t]) continue;
+#pragma unroll
+          for (int t = 0; t < kTiles; ++t) {
+            const int nbt = t ? nb1 : nb0;
+            if (!ok || j >= nbt) continue;
             ok = mbar_wait(bar_p_full(t), j & 1, wc, 6);
-            if (!ok) break;
+            if (!ok) continue;
             tc_fence_after();
             issue_pv(t, j);
-            if (j + 1 < nb[t]) {
+            if (j + 1 < nbt) {
               if (!k_next) {
                 ok = mbar_wait(bar_k_full((j + 1) % C::kStages), ((j + 1) / C::kStages) & 1, wc, 7);
                 k_next = true;
               }
               // S_t(j+1) overwrites P_t(j): wait until P_t(j) V has been consumed
               ok = ok && mbar_wait(bar_pv_done(t), j & 1, wc, 8);
-              if (!ok) break;
+              if (!ok) continue;
               tc_fence_after();
               issue_s(t, j + 1);
             }
@@ -298,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t colS = C::col_s(t), colO = C::col_o(t);
     const float c = p.c;
-    const int my_nb = nb[t];
-    const int my_min_limit = min_limit[t];
+    const int my_nb = t ? nb[1] : nb[0];
+    const int my_min_limit = t ? min_limit[1] : min_limit[0];
+    const bool my_has_rows = t ? has_rows[1] : has_rows[0];
     float m = -INFINITY;  // running max, log2 domain
     float l = 0.f;        // running denominator
     bool ok = true;
@@ -391,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // one decision for the four warps of this tile (the named barriers below need all of them)
     const bool give_up = bar_sync_or(1 + t, 128, !ok || *abort_flag != 0u);
-    if (!give_up && has_rows[t]) {
+    if (!give_up && my_has_rows) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint8_t* orow = smem + C::kOffQ + t * C::kTileBytes + r * 128;
 #pragma unroll
