@@ -114,14 +114,7 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_attr_set[dev][di]) {
-      cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-      if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cudaFuncGetAttributes: %s", cudaGetErrorString(e));
-      // the in-kernel register split assumes exactly this many registers per thread at launch
-      if (fa.numRegs != attn::kLaunchRegs)
-        return fail(ATTN_ERR_LAUNCH, "kernel built with %d registers per thread, expected %d", fa.numRegs,
-                    attn::kLaunchRegs);
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
       if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
       g_attr_set[dev][di] = true;
     }
@@ -143,14 +136,14 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.H = H;
   p.Nq = Nq;
   p.Nk = Nk;
-  p.units_per_bh = (Nq + attn::kRowsPerCta - 1) / attn::kRowsPerCta;
+  p.num_qtiles = (Nq + attn::kBM - 1) / attn::kBM;
   p.causal = causal ? 1 : 0;
   p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.lens = lens;
   p.lse = LSE;
   p.status = status;
   p.timeout_ns = kDefaultTimeoutNs;
-  const unsigned grid = static_cast<unsigned>(p.units_per_bh) * static_cast<unsigned>(BH);
+  const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH);
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));

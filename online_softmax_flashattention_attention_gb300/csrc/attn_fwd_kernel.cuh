@@ -1,21 +1,26 @@
 // Fused attention forward with the online-softmax recurrence, sm_103a.
 //
-// One CTA computes two tiles of 128 query rows (256 consecutive rows) of one
-// (batch, head).  Warp roles:
-//   warps 0-3  softmax of tile 0, warps 4-7 softmax of tile 1: thread t of a group owns
-//              query row t of its tile (tensor-memory lane t).  Per key block it reads
-//              the score row S from tensor memory, masks, takes the block max, computes
-//              alpha and p = exp2(c*s - m), updates l, writes P (bf16) back into tensor
-//              memory over its own S, and rescales the output accumulator o~ by alpha
-//              when any row of its warp saw the max rise.  At the end it divides o~ by
-//              l once and writes O (TMA store) and LSE.
-//   warp 8     MMA issuer: tcgen05.mma S_t = Q_t K^T (both operands in shared memory)
-//              and o~_t += P_t V (P from tensor memory, V from shared memory), alternating
-//              between the two tiles so the tensor core works on one tile while the
-//              other tile's softmax runs.
-//   warp 9     producer: TMA loads of the two Q tiles and of K/V blocks into a ring of
-//              shared-memory stages guarded by full/empty mbarriers.  Both tiles share
-//              each K/V block.
+// One CTA computes one tile of 128 query rows of one (batch, head).  Warp roles:
+//   warps 0-3  softmax: thread r owns query row r of the tile (tensor-memory lane r).
+//              Per key block it reads the score row S from tensor memory, masks, takes
+//              the block max, computes alpha and p = exp2(c*s - m), updates l, writes P
+//              (bf16) back into tensor memory over its own S and rescales the output
+//              accumulator o~ by alpha when some row of its warp saw the max rise.  At the
+//              end it divides o~ by l once and writes O (TMA store) and LSE.
+//   warp 4     producer: TMA loads of the Q tile and of K/V blocks into a ring of
+//              shared-memory stages guarded by full/free mbarriers.
+//   warp 5     P V issuer: tcgen05.mma o~ += P_j V_j (P from tensor memory, V from shared
+//              memory) as soon as the softmax warps have written P_j.
+//   warp 6     S issuer: tcgen05.mma S_j = Q K_j^T (both operands in shared memory) into
+//              score buffer j % 3, as soon as the buffer is free (P_{j-3} V done) and K_j
+//              has landed.
+// Three score buffers let the tensor core compute the next scores while the softmax
+// warps work on S_j.  The two kinds of product come from two issuing warps: issuing a
+// tcgen05.mma blocks while the tensor core is busy, and each issuer spends most of its
+// time waiting on a barrier; with one issuer every such wait left the tensor core idle.
+// One tile per CTA keeps a single busy softmax warp per scheduler partition (measured
+// on GB300, a lightly loaded warp next to two busy warps gets its instructions issued
+// only every 8-14 cycles).
 //
 // The recurrence is the block-wise update of "FlashAttention math" (aicassindra.com),
 // section "The block-wise update, and the full algorithm", and of "2.2b: FlashAttention
@@ -37,27 +42,17 @@
 namespace attn {
 
 constexpr int kBM = 128;           // query rows per tile (= tensor-memory lanes)
-constexpr int kTiles = 2;          // query tiles per CTA
-constexpr int kRowsPerCta = kBM * kTiles;
 constexpr int kBN = 128;           // keys per block
-constexpr int kWarpMma = 8;
-constexpr int kWarpTma = 9;
-constexpr int kThreads = 384;      // 2 softmax warpgroups + a warpgroup holding the MMA and producer warps
+constexpr int kSBufs = 3;          // tensor-memory score buffers
+constexpr int kWarpTma = 4;
+constexpr int kWarpPv = 5;
+constexpr int kWarpS = 6;
+constexpr int kThreads = 224;      // 4 softmax warps + producer + two MMA issuers
 constexpr uint32_t kTmemCols = 512;
-// Register split.  The CTA is launched with kLaunchRegs per thread (384 x 168 = 64512, the
-// most three warps per scheduler partition allow); the MMA/producer warpgroup then gives
-// registers back and the two softmax warpgroups take them:
-// 2 x 128 x 208 + 128 x 88 = 64512.  The host refuses to launch a build whose register
-// count differs from kLaunchRegs, since setmaxnreg.inc would then wait for registers
-// that never come free.
-constexpr int kLaunchRegs = 168;
-constexpr int kSoftmaxRegs = 208;
-constexpr int kOtherRegs = 88;
-static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split");
 
 struct FwdParams {
   int BH, H, Nq, Nk;
-  int units_per_bh;        // ceil(Nq / 256)
+  int num_qtiles;          // ceil(Nq / 128)
   int causal;
   float c;                 // scale * log2(e)
   const int32_t* lens;     // per-batch key lengths or null
@@ -71,22 +66,23 @@ struct FwdCfg {
   static constexpr int kSub = D / 64;                 // 64-column swizzle sub-tiles per row tile
   static constexpr int kSubBytes = 128 * 128;         // 128 rows x 64 bf16 = 16 KiB
   static constexpr int kTileBytes = kSub * kSubBytes; // 128 rows x D bf16
-  static constexpr int kStages = (D == 128) ? 2 : 4;  // K/V ring depth
-  static constexpr int kOffQ = 0;                     // Q tile t at kOffQ + t * kTileBytes
-  static constexpr int kOffK = kTiles * kTileBytes;
+  static constexpr int kStages = (D == 128) ? 3 : 4;  // K/V ring depth
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_full[2], k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  // pv_done[2], mma_done
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 1;
+  // barriers: q_full, k_full[S], v_full[S], k_free[S], v_free[S], s_full[3], pv_done[3],
+  // p_full[3], drain[2]
+  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kSBufs + 2;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack to align the base to 1024 B
-  // tensor-memory columns: S_t (P_t aliases its first 64 columns), then o~_t
-  __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + D * t; }
+  // tensor-memory columns: S buffers b = 0..2 (P aliases the first 64 columns), then o~
+  __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * b; }
+  static constexpr uint32_t kColO = 128u * kSBufs;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, 1);
+  static_assert(kColO + D <= kTmemCols, "tensor memory");
 };
 
 // Visible keys of a row are exactly j < limit(row): both the key padding and the
@@ -112,72 +108,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::kOffQ;
   const uint32_t sK = sbase + C::kOffK;
   const uint32_t sV = sbase + C::kOffV;
   const uint32_t bar0 = sbase + C::kOffBar;
-  auto sQ = [&](int t) { return sbase + C::kOffQ + t * C::kTileBytes; };
-  auto bar_q_full = [&](int t) { return bar0 + 8u * t; };
-  auto bar_k_full = [&](int s) { return bar0 + 8u * (2 + s); };
-  auto bar_k_empty = [&](int s) { return bar0 + 8u * (2 + C::kStages + s); };
-  auto bar_v_full = [&](int s) { return bar0 + 8u * (2 + 2 * C::kStages + s); };
-  auto bar_v_empty = [&](int s) { return bar0 + 8u * (2 + 3 * C::kStages + s); };
-  auto bar_s_full = [&](int t) { return bar0 + 8u * (2 + 4 * C::kStages + t); };
-  auto bar_p_full = [&](int t) { return bar0 + 8u * (4 + 4 * C::kStages + t); };
-  auto bar_pv_done = [&](int t) { return bar0 + 8u * (6 + 4 * C::kStages + t); };
-  const uint32_t bar_mma_done = bar0 + 8u * (8 + 4 * C::kStages);
+  const uint32_t bar_q_full = bar0;
+  auto bar_k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_v_full = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
+  auto bar_k_free = [&](int s) { return bar0 + 8u * (1 + 2 * C::kStages + s); };
+  auto bar_v_free = [&](int s) { return bar0 + 8u * (1 + 3 * C::kStages + s); };
+  auto bar_s_full = [&](int b) { return bar0 + 8u * (1 + 4 * C::kStages + b); };
+  // pv_done[b] completes once per P_j V with j % 3 == b (it also frees score buffer b)
+  auto bar_pv_done = [&](int b) { return bar0 + 8u * (1 + 4 * C::kStages + kSBufs + b); };
+  // p_full[b]: the softmax warps have written P_j (and rescaled o~) for j % 3 == b
+  auto bar_p_full = [&](int b) { return bar0 + 8u * (1 + 4 * C::kStages + 2 * kSBufs + b); };
+  auto bar_drain = [&](int i) { return bar0 + 8u * (1 + 4 * C::kStages + 3 * kSBufs + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: heads in order (their K/V stay in L2 while their units run);
-  //      within a head, causal units longest first
-  const int ub = p.units_per_bh;
-  const int bh = blockIdx.x / ub;
-  int u = blockIdx.x % ub;
-  if (p.causal) u = ub - 1 - u;
+  // ---- work unit: heads in order (their K/V stay in L2 while their tiles run);
+  //      within a head, causal tiles longest first
+  const int nqt = p.num_qtiles;
+  const int bh = blockIdx.x / nqt;
+  int qtile = blockIdx.x % nqt;
+  if (p.causal) qtile = nqt - 1 - qtile;
   const int b = bh / p.H;
-  const int q0 = u * kRowsPerCta;
+  const int q0 = qtile * kBM;
   int kv_len = p.Nk;
   if (p.lens) {
     const int L = __ldg(p.lens + b);
     kv_len = L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
   }
-  // per tile: number of key blocks with a visible key, and the key limit of its first row
-  int nb[kTiles], min_limit[kTiles];
-  bool has_rows[kTiles];
-#pragma unroll
-  for (int t = 0; t < kTiles; ++t) {
-    const int qt0 = q0 + t * kBM;
-    has_rows[t] = qt0 < p.Nq;
-    const int qlast = min(qt0 + kBM - 1, p.Nq - 1);
-    const int max_limit = has_rows[t] ? row_key_limit(qlast, kv_len, p.Nq, p.Nk, p.causal) : 0;
-    min_limit[t] = row_key_limit(qt0, kv_len, p.Nq, p.Nk, p.causal);
-    nb[t] = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;
-  }
-  const int nblk = max(nb[0], nb[1]);
+  const int qlast = min(q0 + kBM - 1, p.Nq - 1);
+  const int max_limit = row_key_limit(qlast, kv_len, p.Nq, p.Nk, p.causal);
+  const int min_limit = row_key_limit(q0, kv_len, p.Nq, p.Nk, p.causal);
+  const int nblk = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;
 
   WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
-    for (int t = 0; t < kTiles; ++t) {
-      mbar_init(bar_q_full(t), 1);
-      mbar_init(bar_s_full(t), 1);
-      mbar_init(bar_p_full(t), 4);
-      mbar_init(bar_pv_done(t), 1);
-    }
+    mbar_init(bar_q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_k_full(s), 1);
-      mbar_init(bar_k_empty(s), 1);
       mbar_init(bar_v_full(s), 1);
-      mbar_init(bar_v_empty(s), 1);
+      mbar_init(bar_k_free(s), 1);
+      mbar_init(bar_v_free(s), 1);
     }
-    mbar_init(bar_mma_done, 1);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(bar_s_full(i), 1);
+      mbar_init(bar_pv_done(i), 1);
+      mbar_init(bar_p_full(i), 4);
+    }
+    mbar_init(bar_drain(0), 1);
+    mbar_init(bar_drain(1), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) tmem_alloc<kTmemCols>(smem_u32(tmem_slot));
+  if (warp == kWarpPv) tmem_alloc<kTmemCols>(smem_u32(tmem_slot));
   if (warp == kWarpTma && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
@@ -189,147 +179,113 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
-    if (warp == kWarpTma) {
-      // ============================================================== producer
-      if (lane == 0 && nblk > 0) {
-        const uint64_t pol_kv = policy_evict_last();
-        const uint64_t pol_q = policy_evict_first();
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) {
-          if (nb[t] == 0) continue;
-          mbar_arrive_expect_tx(bar_q_full(t), C::kTileBytes);
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sQ(t) + s * C::kSubBytes, &tmQ, bar_q_full(t), s * 64, q0 + t * kBM, bh, pol_q);
-        }
-        int k_issued = 0, v_issued = 0;
-        for (int j = 0; j < nblk; ++j) {
-          const int st = j % C::kStages;
-          const uint32_t ph = (j / C::kStages) & 1;
-          if (!mbar_wait(bar_k_empty(st), ph ^ 1, wc, 1)) break;
-          mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, j * kBN, bh,
-                        pol_kv);
-          k_issued = j + 1;
-          if (!mbar_wait(bar_v_empty(st), ph ^ 1, wc, 2)) break;
-          mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64, j * kBN, bh,
-                        pol_kv);
-          v_issued = j + 1;
-        }
-        if (*abort_flag) {
-          // let the copies already issued land before the CTA exits
-          for (int i = (k_issued > C::kStages ? k_issued - C::kStages : 0); i < k_issued; ++i)
-            mbar_wait_drain(bar_k_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
-          for (int i = (v_issued > C::kStages ? v_issued - C::kStages : 0); i < v_issued; ++i)
-            mbar_wait_drain(bar_v_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
-        }
+  if (warp == kWarpTma) {
+    // ================================================================ producer
+    if (lane == 0 && nblk > 0) {
+      const uint64_t pol_kv = policy_evict_last();
+      const uint64_t pol_q = policy_evict_first();
+      mbar_arrive_expect_tx(bar_q_full, C::kTileBytes);
+      for (int s = 0; s < C::kSub; ++s) tma_load_3d(sQ + s * C::kSubBytes, &tmQ, bar_q_full, s * 64, q0, bh, pol_q);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int st = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!mbar_wait(bar_k_free(st), ph ^ 1, wc, 1)) break;
+        mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, j * kBN, bh,
+                      pol_kv);
+        k_issued = j + 1;
+        if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) break;
+        mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64, j * kBN, bh,
+                      pol_kv);
+        v_issued = j + 1;
       }
-    } else if (warp == kWarpMma) {
-      // ============================================================== MMA issuer
-      if (lane == 0 && nblk > 0) {
-        // Shared-memory descriptors: the high word (stride 1024 B, version 1, 128-byte
-        // swizzle) is the same for every operand; the low word holds the start address
-        // (>> 4) and the leading byte offset, so a k-step is one add to the low word.
-        const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
-        const uint32_t qlo0 = (sQ(0) >> 4) | (1u << 16);
-        const uint32_t qlo1 = (sQ(1) >> 4) | (1u << 16);
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA exits
+        for (int i = (k_issued > C::kStages ? k_issued - C::kStages : 0); i < k_issued; ++i)
+          mbar_wait_drain(bar_k_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
+        for (int i = (v_issued > C::kStages ? v_issued - C::kStages : 0); i < v_issued; ++i)
+          mbar_wait_drain(bar_v_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
+      }
+    }
+  } else if (warp == kWarpPv || warp == kWarpS) {
+    // ================================================================ MMA issuers
+    if (lane == 0 && nblk > 0) {
+      // Shared-memory descriptors: the high word (stride 1024 B, version 1, 128-byte
+      // swizzle) is the same for every operand; the low word holds the start address
+      // (>> 4) and the leading byte offset, so a k-step is one add to the low word.
+      const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      bool ok = true;
+      int n = 0;  // products issued by this thread
+      if (warp == kWarpS) {
+        const uint32_t qlo = (sQ >> 4) | (1u << 16);
         const uint32_t klo = (sK >> 4) | (1u << 16);
-        const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
-        const uint32_t ts0 = tmem + C::col_s(0), ts1 = tmem + C::col_s(1);
-        const uint32_t to0 = tmem + C::col_o(0), to1 = tmem + C::col_o(1);
-        const int nb0 = nb[0], nb1 = nb[1];
-        // S_t = Q_t K_j^T: 8 (d = 128) or 4 (d = 64) k-steps of 16
-        auto issue_s = [&](int t, int j) {
-          const uint32_t alo = t ? qlo1 : qlo0;
-          const uint32_t blo = klo + (j % C::kStages) * (C::kTileBytes >> 4);
-          const uint32_t d = t ? ts1 : ts0;
+        ok = mbar_wait(bar_q_full, 0, wc, 3);
+        for (int j = 0; ok && j < nblk; ++j) {
+          const int st = j % C::kStages;
+          const int bf = j % kSBufs;
+          // buffer bf last held P_{j-3}: its P V product must have consumed it
+          if (j >= kSBufs) ok = mbar_wait(bar_pv_done(bf), ((j - kSBufs) / kSBufs) & 1, wc, 4);
+          ok = ok && mbar_wait(bar_k_full(st), (j / C::kStages) & 1, wc, 5);
+          if (!ok) break;
+          tc_fence_after();
+          // S_j = Q K_j^T: 8 (d = 128) or 4 (d = 64) k-steps of 16
+          const uint32_t blo = klo + st * (C::kTileBytes >> 4);
+          const uint32_t d = tmem + C::col_s(bf);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks / 4) * (C::kSubBytes >> 4) + (ks % 4) * 2;
-            mma_ss(d, (static_cast<uint64_t>(dhi) << 32) | (alo + off), (static_cast<uint64_t>(dhi) << 32) | (blo + off),
-                   C::kIdescS, ks > 0 ? 1u : 0u);
+            mma_ss(d, (static_cast<uint64_t>(dhi) << 32) | (qlo + off),
+                   (static_cast<uint64_t>(dhi) << 32) | (blo + off), C::kIdescS, ks > 0 ? 1u : 0u);
           }
-          mma_commit(bar_s_full(t));
-        };
-        // o~_t += P_t V_j: 8 k-steps of 16 keys; A = P_t from tensor memory, B = V_j MN-major
-        auto issue_pv = [&](int t, int j) {
-          const uint32_t blo = vlo + (j % C::kStages) * (C::kTileBytes >> 4);
-          const uint32_t a = t ? ts1 : ts0;
-          const uint32_t d = t ? to1 : to0;
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ts(d, a + ks * 8, (static_cast<uint64_t>(dhi) << 32) | (blo + ks * (16 * 128 >> 4)), C::kIdescO,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar_pv_done(t));
-        };
-        bool ok = mbar_wait(bar_k_full(0), 0, wc, 3);
-        if (ok && nb0 > 0) {
-          ok = mbar_wait(bar_q_full(0), 0, wc, 4);
-          tc_fence_after();
-          if (ok) issue_s(0, 0);
+          mma_commit(bar_s_full(bf));
+          mma_commit(bar_k_free(st));
+          ++n;
         }
-        if (ok && nb1 > 0) {
-          ok = mbar_wait(bar_q_full(1), 0, wc, 4);
-          tc_fence_after();
-          if (ok) issue_s(1, 0);
-        }
-        if (ok) mma_commit(bar_k_empty(0));
+      } else {
+        const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
         for (int j = 0; ok && j < nblk; ++j) {
           const int st = j % C::kStages;
-          ok = mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 5);
-          bool k_next = false;
-#pragma unroll
-          for (int t = 0; t < kTiles; ++t) {
-            const int nbt = t ? nb1 : nb0;
-            if (!ok || j >= nbt) continue;
-            ok = mbar_wait(bar_p_full(t), j & 1, wc, 6);
-            if (!ok) continue;
-            tc_fence_after();
-            issue_pv(t, j);
-            if (j + 1 < nbt) {
-              if (!k_next) {
-                ok = mbar_wait(bar_k_full((j + 1) % C::kStages), ((j + 1) / C::kStages) & 1, wc, 7);
-                k_next = true;
-              }
-              // S_t(j+1) overwrites P_t(j): wait until P_t(j) V has been consumed
-              ok = ok && mbar_wait(bar_pv_done(t), j & 1, wc, 8);
-              if (!ok) continue;
-              tc_fence_after();
-              issue_s(t, j + 1);
-            }
-          }
+          ok = mbar_wait(bar_p_full(j % kSBufs), (j / kSBufs) & 1, wc, 6) &&
+               mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 7);
           if (!ok) break;
-          mma_commit(bar_v_empty(st));
-          if (k_next) mma_commit(bar_k_empty((j + 1) % C::kStages));
+          tc_fence_after();
+          // o~ += P_j V_j: 8 k-steps of 16 keys; A = P_j from tensor memory, B = V_j MN-major
+          const uint32_t blo = vlo + st * (C::kTileBytes >> 4);
+          const uint32_t a = tmem + C::col_s(j % kSBufs);
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            mma_ts(tmem + C::kColO, a + ks * 8, (static_cast<uint64_t>(dhi) << 32) | (blo + ks * (16 * 128 >> 4)),
+                   C::kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(bar_pv_done(j % kSBufs));
+          mma_commit(bar_v_free(st));
+          ++n;
         }
-        // every MMA this thread issued must finish before tensor memory is released
-        mma_commit(bar_mma_done);
-        mbar_wait_drain(bar_mma_done, 0, p.timeout_ns);
       }
+      if (!ok) {
+        // let every MMA this thread issued finish before tensor memory is released
+        mma_commit(bar_drain(warp == kWarpS));
+        mbar_wait_drain(bar_drain(warp == kWarpS), 0, p.timeout_ns);
+      }
+      (void)n;
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ================================================================ softmax / epilogue
-    const int t = warp >> 2;               // tile of this warpgroup
-    const int r = threadIdx.x & 127;       // row within the tile = tensor-memory lane
-    const int row = q0 + t * kBM + r;
+    const int r = threadIdx.x;             // 0..127: row within the tile = tensor-memory lane
+    const int row = q0 + r;
     const int limit = row_key_limit(row, kv_len, p.Nq, p.Nk, p.causal);
-    const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t colS = C::col_s(t), colO = C::col_o(t);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float c = p.c;
-    const int my_nb = t ? nb[1] : nb[0];
-    const int my_min_limit = t ? min_limit[1] : min_limit[0];
-    const bool my_has_rows = t ? has_rows[1] : has_rows[0];
     float m = -INFINITY;  // running max, log2 domain
     float l = 0.f;        // running denominator
     bool ok = true;
-    for (int j = 0; j < my_nb; ++j) {
+    for (int j = 0; j < nblk; ++j) {
+      const uint32_t colS = C::col_s(j % kSBufs);
       // every lane of the warp takes the same branch: the tcgen05 loads below are warp-wide
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(t), j & 1, wc, 9));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(j % kSBufs), (j / kSBufs) & 1, wc, 9));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[kBN];
@@ -340,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k = 0; k < kBN; ++k) s[k] = __uint_as_float(sr[k]);
       const int kb = j * kBN;
-      if (kb + kBN > my_min_limit) {
+      if (kb + kBN > min_limit) {
 #pragma unroll
         for (int k = 0; k < kBN; ++k)
           if (kb + k >= limit) s[k] = -INFINITY;
@@ -383,15 +339,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_new;
       if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
         // o~ may be touched only after the previous P V product has landed in it
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv_done(t), (j - 1) & 1, wc, 10));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, wc, 10));
         if (!ok) break;
         tc_fence_after();
         const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int q = 0; q < D / 64; ++q) {
           uint32_t o[64];
-          tmem_ld32(tl + colO + q * 64, o);
-          tmem_ld32(tl + colO + q * 64 + 32, o + 32);
+          tmem_ld32(tl + C::kColO + q * 64, o);
+          tmem_ld32(tl + C::kColO + q * 64 + 32, o + 32);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
@@ -399,30 +356,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             o[2 * k] = __float_as_uint(v.x);
             o[2 * k + 1] = __float_as_uint(v.y);
           }
-          tmem_st32(tl + colO + q * 64, o);
-          tmem_st32(tl + colO + q * 64 + 32, o + 32);
+          tmem_st32(tl + C::kColO + q * 64, o);
+          tmem_st32(tl + C::kColO + q * 64 + 32, o + 32);
         }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full(t));
+      if (lane == 0) mbar_arrive(bar_p_full(j % kSBufs));
     }
     // ---- epilogue: one division by l, O through shared memory and a TMA store, LSE direct
-    if (ok && my_nb > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv_done(t), (my_nb - 1) & 1, wc, 11));
+    if (ok && nblk > 0) {
+      // the last P V (also the last MMA of the tile) has landed in o~
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar_pv_done((nblk - 1) % kSBufs), ((nblk - 1) / kSBufs) & 1, wc, 11));
       tc_fence_after();
     }
-    // one decision for the four warps of this tile (the named barriers below need all of them)
-    const bool give_up = bar_sync_or(1 + t, 128, !ok || *abort_flag != 0u);
-    if (!give_up && my_has_rows) {
+    // one decision for all four softmax warps (the named barriers below need all of them)
+    const bool give_up = bar_sync_or(1, 128, !ok || *abort_flag != 0u);
+    if (!give_up) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t* orow = smem + C::kOffQ + t * C::kTileBytes + r * 128;
+      uint8_t* orow = smem + C::kOffQ + r * 128;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
-        if (my_nb > 0) {
-          tmem_ld32(tl + colO + q * 32, o);
+        if (nblk > 0) {
+          tmem_ld32(tl + C::kColO + q * 32, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -445,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse;
       }
       fence_proxy_async_smem();
-      bar_sync_named(1 + t, 128);
+      bar_sync_named(1, 128);
       if (r == 0) {
-        for (int s = 0; s < C::kSub; ++s) tma_store_3d(&tmO, sQ(t) + s * C::kSubBytes, s * 64, q0 + t * kBM, bh);
+        for (int s = 0; s < C::kSub; ++s) tma_store_3d(&tmO, sQ + s * C::kSubBytes, s * 64, q0, bh);
         tma_store_commit();
         tma_store_wait_all();
       }
@@ -456,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpPv) {
     tc_fence_after();
     tmem_dealloc<kTmemCols>(tmem);
   }
