@@ -249,8 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
         for (int j = 0; ok && j < nblk; ++j) {
           const int st = j % C::kStages;
-          ok = mbar_wait(bar_p_full(j % kSBufs), (j / kSBufs) & 1, wc, 6) &&
-               mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 7);
+          // V_j has normally landed long before P_j is ready: check it first
+          ok = mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 7) &&
+               mbar_wait(bar_p_full(j % kSBufs), (j / kSBufs) & 1, wc, 6);
           if (!ok) break;
           tc_fence_after();
           // o~ += P_j V_j: 8 k-steps of 16 keys; A = P_j from tensor memory, B = V_j MN-major
@@ -301,16 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kBN; ++k)
           if (kb + k >= limit) s[k] = -INFINITY;
       }
-      // block max: four independent chains of 3-input max over s[0..kBN)
-      float a0 = fmaxf(s[0], s[1]), a1 = fmaxf(s[2], s[3]), a2 = fmaxf(s[4], s[5]), a3 = fmaxf(s[6], s[7]);
+      // block max: eight independent chains of 3-input max over s[0..kBN)
+      float a[8];
 #pragma unroll
-      for (int k = 8; k < kBN; k += 8) {
-        a0 = fmax3(a0, s[k], s[k + 1]);
-        a1 = fmax3(a1, s[k + 2], s[k + 3]);
-        a2 = fmax3(a2, s[k + 4], s[k + 5]);
-        a3 = fmax3(a3, s[k + 6], s[k + 7]);
+      for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmaxf(s[2 * c8], s[2 * c8 + 1]);
+#pragma unroll
+      for (int k = 16; k < kBN; k += 16) {
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmax3(a[c8], s[k + 2 * c8], s[k + 2 * c8 + 1]);
       }
-      const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      const float mx = fmaxf(fmaxf(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5])), fmaxf(a[6], a[7]));
       const float m_new = fmaxf(m, mx * c);
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_ref);

@@ -47,6 +47,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` of barrier `bar`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared state for bounded waits: the first thread whose wait runs out records
 // where in the CTA's abort word and the device status word; every later wait
 // in the CTA sees the abort word and gives up at once.
@@ -57,7 +70,10 @@ struct WaitCtx {
 };
 
 // Wait for phase `parity` of barrier `bar`; false if the wait ran out or the CTA aborted.
+// A phase that has already completed is found with the non-blocking test; only a
+// pending phase goes to try_wait, which may suspend the thread until it completes.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  if (mbar_test_wait(bar, parity)) return true;
 #pragma unroll 1
   for (int i = 0; i < 64; ++i)
     if (mbar_try_wait(bar, parity)) return true;
