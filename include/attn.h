@@ -66,6 +66,11 @@ typedef enum {
  *   stream    a cudaStream_t, or NULL for the legacy default stream.
  * Asynchronous: returns after the launch.  Argument and launch errors are returned at
  * once; a device-side wait timeout is reported by attn_status_sync.
+ * Environment, read at every launch (all entry points):
+ *   ATTN_WAIT_LIMIT_MS          limit of each device-side wait in ms (default 2000).
+ *   ATTN_TEST_WITHHOLD_K_BLOCK  test hook only: the loader skips key block j (0-based) of
+ *                               every tile, so the waits on it run out; the call then
+ *                               reports ATTN_ERR_TIMEOUT and O / LSE are not written.
  */
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                      int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, void* stream);

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -85,6 +86,24 @@ attn_status make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
   return ATTN_OK;
 }
 
+// Limit of every bounded device-side wait: ATTN_WAIT_LIMIT_MS when set (> 0), else 2 s.
+unsigned long long wait_limit_ns() {
+  const char* v = std::getenv("ATTN_WAIT_LIMIT_MS");
+  if (v && *v) {
+    const long ms = std::strtol(v, nullptr, 10);
+    if (ms > 0) return static_cast<unsigned long long>(ms) * 1000000ull;
+  }
+  return kDefaultTimeoutNs;
+}
+
+// Test hook: ATTN_TEST_WITHHOLD_K_BLOCK=j makes every CTA's producer skip the load of key
+// block j, so the waits on it run out and the failure path can be exercised without a fault.
+int fault_block() {
+  const char* v = std::getenv("ATTN_TEST_WITHHOLD_K_BLOCK");
+  if (v && *v) return static_cast<int>(std::strtol(v, nullptr, 10));
+  return -1;
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 attn_status check_args(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
@@ -142,7 +161,8 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.lens = lens;
   p.lse = LSE;
   p.status = status;
-  p.timeout_ns = kDefaultTimeoutNs;
+  p.timeout_ns = wait_limit_ns();
+  p.fault_block = fault_block();
   const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH);
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   cudaError_t e = cudaGetLastError();

@@ -59,6 +59,7 @@ struct FwdParams {
   float* lse;              // [BH, Nq]
   uint32_t* status;        // device status word (bit 0: a wait ran out)
   unsigned long long timeout_ns;
+  int fault_block;         // test hook: the K block the producer never loads (-1: none)
 };
 
 template <int D>
@@ -191,10 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
         if (!mbar_wait(bar_k_free(st), ph ^ 1, wc, 1)) break;
-        mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, j * kBN, bh,
-                      pol_kv);
+        if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
+          mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, j * kBN, bh,
+                        pol_kv);
+        }
         k_issued = j + 1;
         if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) break;
         mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
@@ -203,13 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       pol_kv);
         v_issued = j + 1;
       }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA exits
-        for (int i = (k_issued > C::kStages ? k_issued - C::kStages : 0); i < k_issued; ++i)
-          mbar_wait_drain(bar_k_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
-        for (int i = (v_issued > C::kStages ? v_issued - C::kStages : 0); i < v_issued; ++i)
-          mbar_wait_drain(bar_v_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
-      }
+      // Let the last copies issued land before this warp leaves (in a normal run they were
+      // consumed long ago; after a failed wait nobody else will wait for them).
+      for (int i = (k_issued > C::kStages ? k_issued - C::kStages : 0); i < k_issued; ++i)
+        if (i != p.fault_block) mbar_wait_drain(bar_k_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
+      for (int i = (v_issued > C::kStages ? v_issued - C::kStages : 0); i < v_issued; ++i)
+        mbar_wait_drain(bar_v_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
     }
   } else if (warp == kWarpPv || warp == kWarpS) {
     // ================================================================ MMA issuers
@@ -219,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (>> 4) and the leading byte offset, so a k-step is one add to the low word.
       const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
       bool ok = true;
-      int n = 0;  // products issued by this thread
       if (warp == kWarpS) {
         const uint32_t qlo = (sQ >> 4) | (1u << 16);
         const uint32_t klo = (sK >> 4) | (1u << 16);
@@ -243,7 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(bar_s_full(bf));
           mma_commit(bar_k_free(st));
-          ++n;
         }
       } else {
         const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
@@ -263,15 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    C::kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
           mma_commit(bar_pv_done(j % kSBufs));
           mma_commit(bar_v_free(st));
-          ++n;
         }
       }
-      if (!ok) {
-        // let every MMA this thread issued finish before tensor memory is released
-        mma_commit(bar_drain(warp == kWarpS));
-        mbar_wait_drain(bar_drain(warp == kWarpS), 0, p.timeout_ns);
-      }
-      (void)n;
+      // every MMA this thread issued must finish before tensor memory is released (in a
+      // normal run they have: the softmax warps consumed them)
+      mma_commit(bar_drain(warp == kWarpS));
+      mbar_wait_drain(bar_drain(warp == kWarpS), 0, p.timeout_ns);
     }
   } else {
     // ================================================================ softmax / epilogue
