@@ -33,7 +33,8 @@ Readings where the pages are silent (each is listed in the design notes):
 * LSE = m + ln(l) of the scaled scores; the pages name "logsumexp" but define
   only m and l ([OS] "The Sum of Exponentials").
 
-Every function is pinned by tests in ``tests/test_oracle.py`` against the
+Every function is pinned by tests in ``tests/test_oracle.py`` and
+``tests/test_oracle_states.py`` (partial states and their merge) against the
 pages' printed examples, closed forms and brute force.
 """
 from __future__ import annotations
@@ -182,6 +183,115 @@ def attention_rows(Q, K, V, scale: float, causal: bool, lens, picks):
             O[r] = (p @ v) / l
             LSE[r] = m + np.log(l)
     return O, LSE
+
+
+# --- partial states over a key range, and their merge ---------------------------
+
+def attention_state_head(q, k, v, scale: float, causal: bool, key_len, key_begin: int, key_end: int):
+    """The running state (m, l, o~) of every row of one head after absorbing exactly
+    the visible keys j with key_begin <= j < key_end, in float64.
+
+    [FM] "The running state": m = max of the scores seen, l = sum exp(s_j - m) and
+    o~ = sum exp(s_j - m) v_j over the scores seen (o~ unnormalised).  Written from
+    that definition directly (one max, one sum), not through the block loop.  A row
+    that saw no visible key in the range has the initial state m = -inf, l = 0, o~ = 0
+    ([FM] "The block-wise update, and the full algorithm", init line).
+
+    Returns (o_acc [Nq, dv], m [Nq], l [Nq]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    Nq, Nk, dv = q.shape[0], k.shape[0], v.shape[1]
+    o_acc = np.zeros((Nq, dv))
+    m = np.full(Nq, NEG_INF)
+    l = np.zeros(Nq)
+    lo, hi = max(int(key_begin), 0), min(int(key_end), Nk)
+    if Nq == 0 or hi <= lo:
+        return o_acc, m, l
+    s = scale * (q @ k[lo:hi].T)
+    s = np.where(visible(Nq, Nk, causal, key_len)[:, lo:hi], s, NEG_INF)
+    mm = s.max(axis=1)
+    live = mm > NEG_INF
+    ref = np.where(live, mm, 0.0)
+    p = np.exp(s - ref[:, None])
+    m[live] = mm[live]
+    l[live] = p[live].sum(axis=1)
+    o_acc[live] = p[live] @ v[lo:hi]
+    return o_acc, m, l
+
+
+def merge_states(states, _mutation=None):
+    """Combine states (o~_s, m_s, l_s) of disjoint key sets into the state of their union.
+
+    Each state is already expressed relative to its own max m_s.  The rescaling
+    identity of [FM] "The rescaling identity, derived" moves every one of them to the
+    common reference m = max_s m_s with the factor exp(m_s - m) <= 1:
+        l = sum_s exp(m_s - m) l_s,   o~ = sum_s exp(m_s - m) o~_s.
+    The pages state that keys may be absorbed in any order and in blocks of any size
+    ([FM] "The running state"; "Proof of exactness"); a state is such a summary of a
+    block, so the identity applies to it as it does to one block.  If every m_s is
+    -inf the union saw no visible key: (0, -inf, 0).
+
+    states: list of (o_acc [..., dv], m [...], l [...]).  Returns (o_acc, m, l).
+    ``_mutation`` plants a known mistake for the tests that check a pin catches it:
+    "rescale_l_only" (o~_s added without its factor) or "no_rescale" (neither l_s nor
+    o~_s rescaled).
+    """
+    if not states:
+        raise ValueError("merge_states needs at least one state")
+    ms = np.stack([np.asarray(st[1], dtype=np.float64) for st in states])
+    m = ms.max(axis=0)
+    ref = np.where(m > NEG_INF, m, 0.0)
+    o_acc = np.zeros_like(np.asarray(states[0][0], dtype=np.float64))
+    l = np.zeros_like(m)
+    for o_s, m_s, l_s in states:
+        w = np.exp(np.asarray(m_s, dtype=np.float64) - ref)     # exp(-inf) = 0 for an empty state
+        wo = w
+        if _mutation == "no_rescale":
+            w = wo = np.ones_like(w)
+        elif _mutation == "rescale_l_only":
+            wo = np.ones_like(w)
+        l = l + w * np.asarray(l_s, dtype=np.float64)
+        o_acc = o_acc + wo[..., None] * np.asarray(o_s, dtype=np.float64)
+    return o_acc, m, l
+
+
+def finish_state(o_acc, m, l):
+    """O = o~ / l and LSE = m + ln l: the single final division of [FM] "The block-wise
+    update, and the full algorithm"; a state that saw no visible key (l = 0) gives the
+    fully masked convention O = 0, LSE = -inf."""
+    o_acc = np.asarray(o_acc, dtype=np.float64)
+    m = np.asarray(m, dtype=np.float64)
+    l = np.asarray(l, dtype=np.float64)
+    live = l > 0.0
+    O = np.zeros_like(o_acc)
+    LSE = np.full(m.shape, NEG_INF)
+    O[live] = o_acc[live] / l[live][..., None]
+    LSE[live] = m[live] + np.log(l[live])
+    return O, LSE
+
+
+def attention_states(Q, K, V, scale: float, causal: bool, lens, key_ranges):
+    """Batched ``attention_state_head`` for a list of key ranges [(begin, end), ...].
+
+    Q [B,H,Nq,d], K/V [B,H,Nk,d] as bf16 codes or floats.  Returns float64
+    o_acc [S,B,H,Nq,dv], m [S,B,H,Nq], l [S,B,H,Nq] with S = len(key_ranges).
+    """
+    Qf, Kf, Vf = (_as_f64(x) for x in (Q, K, V))
+    B, H, Nq, _ = Qf.shape
+    dv = Vf.shape[3]
+    S = len(key_ranges)
+    o_acc = np.zeros((S, B, H, Nq, dv))
+    m = np.full((S, B, H, Nq), NEG_INF)
+    l = np.zeros((S, B, H, Nq))
+    for si, (lo, hi) in enumerate(key_ranges):
+        for b in range(B):
+            L = None if lens is None else int(lens[b])
+            for h in range(H):
+                o_acc[si, b, h], m[si, b, h], l[si, b, h] = attention_state_head(
+                    Qf[b, h], Kf[b, h], Vf[b, h], scale, causal, L, lo, hi)
+    return o_acc, m, l
 
 
 def _as_f64(x) -> np.ndarray:
