@@ -163,6 +163,10 @@ WORKLOADS = {
             v=("normal", 0.0, 0.5), seed=1005),
         _wl(name="causal_b1h32n32768d64", B=1, H=32, Nq=32768, d=64, causal=True, qk=("normal", 0.0, 0.5),
             v=("normal", 0.0, 0.5), seed=1006),
+        # few query rows over a long key sequence (decoding a chunk of 128 tokens against a
+        # 32K cache, bottom-right causal): 32 query tiles for 152 SMs, the split-KV shape
+        _wl(name="causal_b1h32q128k32768d128", B=1, H=32, Nq=128, Nk=32768, d=128, causal=True,
+            qk=("normal", 0.0, 0.5), v=("normal", 0.0, 0.5), seed=1007),
     ]
 }
 

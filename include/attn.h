@@ -37,6 +37,7 @@
 #ifndef ATTN_H_
 #define ATTN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -131,6 +132,72 @@ int attn_version(void);
 attn_status attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                              int Nq, int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
                              int check_status, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Split-KV: the keys of every row are cut into splits, each split is absorbed into its
+ * own running state, and the states are merged.
+ *
+ * A state is the triple the recurrence carries ("FlashAttention math", section "The
+ * running state"): m = the largest visible scaled score scale * q . k_j of the split,
+ * l = sum exp(s_j - m) and o~ = sum exp(s_j - m) v_j (unnormalised) over the split's
+ * visible keys.  A split with no visible key for a row holds the initial state
+ * m = -inf, l = 0, o~ = 0.  The pages let keys be absorbed in any order and in blocks of
+ * any size (same page, "Proof of exactness"); states of disjoint key sets combine with
+ * the rescaling identity (section "The rescaling identity, derived"): with
+ * m = max_s m_s, l = sum_s exp(m_s - m) l_s and o~ = sum_s exp(m_s - m) o~_s.
+ * This serves shapes with few query tiles and many keys (decoding, short prompts over
+ * a long cache), where one CTA per query tile leaves most SMs idle; the same merge is
+ * the exchange step of a key-sharded (context-parallel) forward.
+ * ------------------------------------------------------------------------------------ */
+
+/*
+ * attn_fwd_states -- the partial states of num_splits key splits (1 <= num_splits <= 256).
+ *   Split s covers keys [s * C, (s + 1) * C) intersected with [0, Nk), where
+ *   C = 128 * ceil(ceil(Nk / 128) / num_splits); masks as for attn_fwd.
+ *   Q, K, V, B, H, Nq, Nk, d, scale, causal, key_padding_lens, stream: as attn_fwd.
+ *   o_states  device fp32 [num_splits, B, H, Nq, d]: o~.
+ *   m_states  device fp32 [num_splits, B, H, Nq]: m (natural-log units; -inf = empty).
+ *   l_states  device fp32 [num_splits, B, H, Nq]: l.
+ *   All three 16-byte aligned.  Asynchronous; timeouts through attn_status_sync.
+ *   Errors: as attn_fwd, plus ATTN_ERR_BAD_ARG for num_splits out of range.
+ */
+attn_status attn_fwd_states(const void* Q, const void* K, const void* V, float* o_states, float* m_states,
+                            float* l_states, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                            const int32_t* key_padding_lens, int num_splits, void* stream);
+
+/*
+ * attn_merge_states -- merge num_states >= 1 states per row and finish each row:
+ *   O = o~ / l (bf16) and LSE = m + ln l, or O = 0 and LSE = -inf when every state of
+ *   the row is empty.  rows = number of rows (B * H * Nq for attn_fwd_states' output).
+ *   o_states fp32 [num_states, rows, d] (16-byte aligned), m_states and l_states fp32
+ *   [num_states, rows], O bf16 [rows, d] (16-byte aligned), LSE fp32 [rows]; all device.
+ *   The states may come from anywhere (another GPU's keys, a previous call).
+ *   Asynchronous on `stream`.  Errors: NULLPTR, MISALIGNED, UNSUPPORTED_D, BAD_ARG
+ *   (num_states < 1), BAD_SHAPE (rows < 0), LAUNCH.
+ */
+attn_status attn_merge_states(const float* o_states, const float* m_states, const float* l_states, int num_states,
+                              long long rows, int d, void* O, float* LSE, void* stream);
+
+/* Bytes of device workspace attn_fwd_splitkv needs for num_splits splits (0 for
+ * invalid arguments): the three state arrays, each rounded up to 256 bytes. */
+size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/* The split count attn_fwd_splitkv picks when given num_splits <= 0, on the current
+ * device: 1 when the query tiles alone fill the SMs, else enough splits to fill them
+ * once, at most one split per four key blocks and at most 256. */
+int attn_splitkv_splits(int B, int H, int Nq, int Nk);
+
+/*
+ * attn_fwd_splitkv -- attn_fwd computed as attn_fwd_states + attn_merge_states.
+ *   Same arguments and result as attn_fwd (within the same tolerance, not bitwise),
+ *   plus num_splits (<= 0: attn_splitkv_splits' choice) and a caller-owned device
+ *   workspace of at least attn_splitkv_workspace_bytes(B, H, Nq, d, splits) bytes,
+ *   16-byte aligned.  With one split the call is attn_fwd and the workspace is unused.
+ *   No allocation.  Asynchronous; ATTN_ERR_BAD_ARG if the workspace is too small.
+ */
+attn_status attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                             int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, int num_splits,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

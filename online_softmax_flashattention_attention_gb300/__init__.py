@@ -15,7 +15,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn.so")
 
 EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
-           "attn_version", "attn_fwd_noalloc")
+           "attn_version", "attn_fwd_noalloc", "attn_fwd_states", "attn_merge_states",
+           "attn_splitkv_workspace_bytes", "attn_splitkv_splits", "attn_fwd_splitkv")
 
 STATUS_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_NULLPTR", -2: "ATTN_ERR_BAD_SHAPE", -3: "ATTN_ERR_UNSUPPORTED_D",
                 -4: "ATTN_ERR_MISALIGNED", -5: "ATTN_ERR_NO_DEVICE", -6: "ATTN_ERR_LAUNCH", -7: "ATTN_ERR_TIMEOUT",
@@ -51,6 +52,16 @@ def load_library():
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_version.argtypes = []
         lib.attn_version.restype = i
+        lib.attn_fwd_states.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
+        lib.attn_fwd_states.restype = i
+        lib.attn_merge_states.argtypes = [vp, vp, vp, i, ctypes.c_longlong, i, vp, vp, vp]
+        lib.attn_merge_states.restype = i
+        lib.attn_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_splitkv_splits.argtypes = [i, i, i, i]
+        lib.attn_splitkv_splits.restype = i
+        lib.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_splitkv.restype = i
         _lib = lib
     return _lib
 
@@ -72,6 +83,38 @@ def attn_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, ca
     lib = load_library()
     return lib.attn_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, int(causal), lens_ptr,
                         stream_ptr)
+
+
+def _check_qkv(Q, K, V, key_padding_lens):
+    """Shapes, dtypes and placement of the inputs; returns (B, H, Nq, Nk, d, lens_ptr)."""
+    import torch
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if K.shape != (B, H, Nk, d) or V.shape != (B, H, Nk, d):
+        raise ValueError("K and V must be [B, H, Nk, d] with Q's B, H and d")
+    lens_ptr = None
+    if key_padding_lens is not None:
+        if key_padding_lens.dtype != torch.int32 or not key_padding_lens.is_cuda or key_padding_lens.numel() != B:
+            raise ValueError("key_padding_lens must be an int32 CUDA tensor [B]")
+        lens_ptr = key_padding_lens.data_ptr()
+    return B, H, Nq, Nk, d, lens_ptr
+
+
+def _outputs(Q, O, LSE):
+    import torch
+    B, H, Nq, _ = Q.shape
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
+    if O.shape != Q.shape or O.dtype != torch.bfloat16 or not O.is_contiguous():
+        raise ValueError("O must be a contiguous bf16 tensor shaped like Q")
+    if LSE.shape != (B, H, Nq) or LSE.dtype != torch.float32 or not LSE.is_contiguous():
+        raise ValueError("LSE must be a contiguous fp32 tensor [B, H, Nq]")
+    return O, LSE
 
 
 def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding_lens=None, stream=None):
@@ -136,3 +179,79 @@ def release_workspace():
 
 def version() -> int:
     return load_library().attn_version()
+
+
+# --- split-KV: partial states and their merge ---------------------------------
+
+def attn_fwd_states(Q, K, V, num_splits, *, scale=None, causal=False, key_padding_lens=None, stream=None):
+    """The running states (o~, m, l) of ``num_splits`` key splits (split s covers keys
+    [s*C, (s+1)*C), C = 128 * ceil(ceil(Nk/128) / num_splits)).  Returns fp32 CUDA tensors
+    o_states [S,B,H,Nq,d], m_states [S,B,H,Nq], l_states [S,B,H,Nq]."""
+    import torch
+    B, H, Nq, Nk, d, lens_ptr = _check_qkv(Q, K, V, key_padding_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    S = int(num_splits)
+    o_st = torch.empty((S, B, H, Nq, d), dtype=torch.float32, device=Q.device)
+    m_st = torch.empty((S, B, H, Nq), dtype=torch.float32, device=Q.device)
+    l_st = torch.empty((S, B, H, Nq), dtype=torch.float32, device=Q.device)
+    rc = load_library().attn_fwd_states(Q.data_ptr(), K.data_ptr(), V.data_ptr(), o_st.data_ptr(), m_st.data_ptr(),
+                                        l_st.data_ptr(), B, H, Nq, Nk, d, float(scale), int(causal), lens_ptr, S,
+                                        _stream_handle(stream))
+    _check(rc)
+    return o_st, m_st, l_st
+
+
+def merge_states(o_states, m_states, l_states, O=None, LSE=None, *, stream=None):
+    """Merge S states per row: o_states fp32 [S, ..., d], m_states / l_states fp32 [S, ...].
+    Returns O bf16 [..., d] and LSE fp32 [...] (allocated when not given)."""
+    import torch
+    S, d = o_states.shape[0], o_states.shape[-1]
+    rows_shape = tuple(o_states.shape[1:-1])
+    for name, t in (("o_states", o_states), ("m_states", m_states), ("l_states", l_states)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+    if tuple(m_states.shape) != (S,) + rows_shape or tuple(l_states.shape) != (S,) + rows_shape:
+        raise ValueError("m_states and l_states must be [S, ...] matching o_states [S, ..., d]")
+    if O is None:
+        O = torch.empty(rows_shape + (d,), dtype=torch.bfloat16, device=o_states.device)
+    if LSE is None:
+        LSE = torch.empty(rows_shape, dtype=torch.float32, device=o_states.device)
+    rows = int(math.prod(rows_shape))
+    if O.numel() != rows * d or O.dtype != torch.bfloat16 or LSE.numel() != rows or LSE.dtype != torch.float32:
+        raise ValueError("O must be bf16 [..., d] and LSE fp32 [...] over the states' rows")
+    rc = load_library().attn_merge_states(o_states.data_ptr(), m_states.data_ptr(), l_states.data_ptr(), S, rows, d,
+                                          O.data_ptr(), LSE.data_ptr(), _stream_handle(stream))
+    _check(rc)
+    return O, LSE
+
+
+def splitkv_splits(B, H, Nq, Nk) -> int:
+    """The split count attn_fwd_splitkv picks for num_splits <= 0 on the current device."""
+    return load_library().attn_splitkv_splits(B, H, Nq, Nk)
+
+
+def splitkv_workspace_bytes(B, H, Nq, d, num_splits) -> int:
+    return load_library().attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+
+
+def attn_fwd_splitkv(Q, K, V, O=None, LSE=None, *, num_splits=0, workspace=None, scale=None, causal=False,
+                     key_padding_lens=None, stream=None):
+    """attn_fwd through split-KV states and their merge.  workspace: a CUDA uint8 tensor
+    of at least splitkv_workspace_bytes(...) bytes, allocated here when not given."""
+    import torch
+    B, H, Nq, Nk, d, lens_ptr = _check_qkv(Q, K, V, key_padding_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    O, LSE = _outputs(Q, O, LSE)
+    S = int(num_splits) if num_splits and num_splits > 0 else splitkv_splits(B, H, Nq, Nk)
+    need = splitkv_workspace_bytes(B, H, Nq, d, S) if S > 1 else 0
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().attn_fwd_splitkv(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H,
+                                         Nq, Nk, d, float(scale), int(causal), lens_ptr, S, ws_ptr, ws_bytes,
+                                         _stream_handle(stream))
+    _check(rc)
+    return O, LSE

@@ -10,10 +10,12 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_merge_kernel.cuh"
 
 namespace {
 
@@ -32,7 +34,8 @@ attn_status fail(attn_status st, const char* fmt, ...) {
 
 std::mutex g_mu;
 uint32_t* g_status[kMaxDevices] = {};
-bool g_attr_set[kMaxDevices][2] = {};
+bool g_attr_set[kMaxDevices][4] = {};
+int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 struct Workspace {
@@ -68,6 +71,7 @@ attn_status setup(int dev, uint32_t** status) {
     if (cudaMalloc(&s, sizeof(uint32_t)) != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "status word alloc failed");
     if (cudaMemset(s, 0, sizeof(uint32_t)) != cudaSuccess) return fail(ATTN_ERR_NO_DEVICE, "status word init failed");
     g_status[dev] = s;
+    g_sms[dev] = prop.multiProcessorCount;
   }
   *status = g_status[dev];
   return ATTN_OK;
@@ -124,12 +128,21 @@ attn_status check_args(const void* Q, const void* K, const void* V, void* O, flo
   return ATTN_OK;
 }
 
-template <int D>
+// Where a partial-state launch writes: o~ [S, BH, Nq, D], m and l [S, BH, Nq], all fp32.
+struct StateOut {
+  float* o = nullptr;
+  float* m = nullptr;
+  float* l = nullptr;
+  int num_splits = 1;
+};
+
+template <int D, bool kStates>
 attn_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
-                   float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status) {
+                   float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
+                   const StateOut& so = StateOut{}) {
   using C = attn::FwdCfg<D>;
-  auto kernel = attn::attn_fwd_kernel<D>;
-  const int di = (D == 128) ? 1 : 0;
+  auto kernel = attn::attn_fwd_kernel<D, kStates>;
+  const int di = ((D == 128) ? 1 : 0) + (kStates ? 2 : 0);
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_attr_set[dev][di]) {
@@ -142,7 +155,11 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   CUtensorMap mq, mk, mv, mo;
   attn_status st;
   if ((st = make_map(&mq, Q, BH, Nq, D)) != ATTN_OK) return st;
-  if ((st = make_map(&mo, O, BH, Nq, D)) != ATTN_OK) return st;
+  if (kStates) {
+    mo = mq;  // never used: the partial-state epilogue stores with plain writes
+  } else if ((st = make_map(&mo, O, BH, Nq, D)) != ATTN_OK) {
+    return st;
+  }
   if (Nk > 0) {
     if ((st = make_map(&mk, K, BH, Nk, D)) != ATTN_OK) return st;
     if ((st = make_map(&mv, V, BH, Nk, D)) != ATTN_OK) return st;
@@ -163,7 +180,14 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.status = status;
   p.timeout_ns = wait_limit_ns();
   p.fault_block = fault_block();
-  const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH);
+  const int nkb = (Nk + attn::kBN - 1) / attn::kBN;
+  p.num_splits = kStates ? so.num_splits : 1;
+  p.split_blocks = kStates ? std::max(1, (nkb + so.num_splits - 1) / so.num_splits) : std::max(1, nkb);
+  p.st_o = so.o;
+  p.st_m = so.m;
+  p.st_l = so.l;
+  const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH) *
+                        static_cast<unsigned>(p.num_splits);
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
@@ -185,8 +209,9 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
   uint32_t* status = nullptr;
   if ((st = setup(dev, &status)) != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 128) return launch<128>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
-  return launch<64>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
+  if (d == 128)
+    return launch<128, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
+  return launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
 }
 
 attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
@@ -333,8 +358,8 @@ extern "C" attn_status attn_fwd_noalloc(const void* Q, const void* K, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(scratch, 0, need, s);  // the array keeps the previous call's word
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
-  st = (d == 128) ? launch<128>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch)
-                  : launch<64>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch);
+  st = (d == 128) ? launch<128, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch)
+                  : launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch);
   if (st != ATTN_OK || !check_status) return st;
   uint32_t word = 0;
   e = cudaStreamSynchronize(s);
@@ -343,3 +368,144 @@ extern "C" attn_status attn_fwd_noalloc(const void* Q, const void* K, const void
   if (word) return fail(ATTN_ERR_TIMEOUT, "a bounded device wait ran out (status word 0x%x)", word);
   return ATTN_OK;
 }
+
+// ---------------------------------------------------------------------------------------
+// Split-KV: partial states over key splits, and their merge.
+
+namespace {
+
+constexpr int kMaxSplits = 256;
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+attn_status launch_merge(const float* o_st, const float* m_st, const float* l_st, int S, long long rows, int d,
+                         void* O, float* LSE, cudaStream_t stream, int sms) {
+  attn::MergeParams mp;
+  mp.st_o = o_st;
+  mp.st_m = m_st;
+  mp.st_l = l_st;
+  mp.S = S;
+  mp.rows = rows;
+  mp.O = static_cast<__nv_bfloat16*>(O);
+  mp.lse = LSE;
+  constexpr long long kRowsPerBlock = attn::kMergeThreads / 32;
+  const long long want = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(want, static_cast<long long>(sms) * 8));
+  if (d == 128)
+    attn::attn_merge_kernel<128><<<grid, attn::kMergeThreads, 0, stream>>>(mp);
+  else
+    attn::attn_merge_kernel<64><<<grid, attn::kMergeThreads, 0, stream>>>(mp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "merge launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+// The automatic split count: enough (unit, split) CTAs to fill the SMs once when the
+// units alone do not, never more splits than key blocks / 4 (each split keeps at least
+// four blocks of work to amortise its start-up) and never more than kMaxSplits.
+int auto_splits(long long units, int nkb, int sms) {
+  if (units <= 0 || units >= sms) return 1;
+  long long s = sms / units;
+  s = std::min<long long>(s, std::max(1, nkb / 4));
+  s = std::min<long long>(s, kMaxSplits);
+  return static_cast<int>(std::max<long long>(1, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_states(const void* Q, const void* K, const void* V, float* o_states, float* m_states,
+                            float* l_states, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                            const int32_t* key_padding_lens, int num_splits, void* stream) {
+  g_err[0] = '\0';
+  attn_status st = check_args(Q, K, V, o_states, m_states, B, H, Nq, Nk, d, scale);
+  if (st != ATTN_OK) return st;
+  if (num_splits < 1 || num_splits > kMaxSplits)
+    return fail(ATTN_ERR_BAD_ARG, "num_splits=%d; must be in [1, %d]", num_splits, kMaxSplits);
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  if (!l_states) return fail(ATTN_ERR_NULLPTR, "l_states must not be NULL");
+  if (misaligned(l_states)) return fail(ATTN_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  const long long units = static_cast<long long>(B) * H * ((Nq + attn::kBM - 1) / attn::kBM);
+  if (units * num_splits > INT32_MAX) return fail(ATTN_ERR_BAD_SHAPE, "too many (tile, split) units");
+  int dev;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  uint32_t* status = nullptr;
+  if ((st = setup(dev, &status)) != ATTN_OK) return st;
+  StateOut so;
+  so.o = o_states;
+  so.m = m_states;
+  so.l = l_states;
+  so.num_splits = num_splits;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    return launch<128, true>(Q, K, V, nullptr, nullptr, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
+                             so);
+  return launch<64, true>(Q, K, V, nullptr, nullptr, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
+                          so);
+}
+
+attn_status attn_merge_states(const float* o_states, const float* m_states, const float* l_states, int num_states,
+                              long long rows, int d, void* O, float* LSE, void* stream) {
+  g_err[0] = '\0';
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED_D, "d=%d; supported: 64, 128", d);
+  if (num_states < 1) return fail(ATTN_ERR_BAD_ARG, "num_states=%d; must be >= 1", num_states);
+  if (rows < 0) return fail(ATTN_ERR_BAD_SHAPE, "rows=%lld must be >= 0", rows);
+  if (rows == 0) return ATTN_OK;
+  if (!o_states || !m_states || !l_states || !O || !LSE)
+    return fail(ATTN_ERR_NULLPTR, "state and output pointers must not be NULL");
+  if (misaligned(o_states) || misaligned(O) || (reinterpret_cast<uintptr_t>(m_states) & 3u) ||
+      (reinterpret_cast<uintptr_t>(l_states) & 3u) || (reinterpret_cast<uintptr_t>(LSE) & 3u))
+    return fail(ATTN_ERR_MISALIGNED, "o_states and O must be 16-byte aligned, m, l and LSE 4-byte aligned");
+  int dev;
+  attn_status st = get_device(&dev);
+  if (st != ATTN_OK) return st;
+  uint32_t* status = nullptr;
+  if ((st = setup(dev, &status)) != ATTN_OK) return st;
+  return launch_merge(o_states, m_states, l_states, num_states, rows, d, O, LSE, static_cast<cudaStream_t>(stream),
+                      g_sms[dev]);
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 0 || H < 0 || Nq < 0 || (d != 64 && d != 128) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq * num_splits;
+  return round256(rows * d * 4) + 2 * round256(rows * 4);
+}
+
+int attn_splitkv_splits(int B, int H, int Nq, int Nk) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk < 0) return 1;
+  int dev;
+  if (get_device(&dev) != ATTN_OK) return 1;
+  uint32_t* status = nullptr;
+  if (setup(dev, &status) != ATTN_OK) return 1;
+  const long long units = static_cast<long long>(B) * H * ((Nq + attn::kBM - 1) / attn::kBM);
+  return auto_splits(units, (Nk + attn::kBN - 1) / attn::kBN, g_sms[dev]);
+}
+
+attn_status attn_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                             int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, int num_splits,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  g_err[0] = '\0';
+  attn_status st = check_args(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+  if (st != ATTN_OK) return st;
+  if (num_splits > kMaxSplits) return fail(ATTN_ERR_BAD_ARG, "num_splits=%d > %d", num_splits, kMaxSplits);
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  const int S = num_splits >= 1 ? num_splits : attn_splitkv_splits(B, H, Nq, Nk);
+  if (S == 1) return attn_fwd(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale, causal, key_padding_lens, stream);
+  const size_t need = attn_splitkv_workspace_bytes(B, H, Nq, d, S);
+  if (!workspace) return fail(ATTN_ERR_NULLPTR, "workspace must not be NULL for %d splits", S);
+  if (misaligned(workspace)) return fail(ATTN_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_BAD_ARG, "workspace of %zu B is smaller than the %zu B %d splits need", workspace_bytes,
+                need, S);
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  float* o_st = reinterpret_cast<float*>(w);
+  float* m_st = reinterpret_cast<float*>(w + round256(rows * S * d * 4));
+  float* l_st = reinterpret_cast<float*>(w + round256(rows * S * d * 4) + round256(rows * S * 4));
+  st = attn_fwd_states(Q, K, V, o_st, m_st, l_st, B, H, Nq, Nk, d, scale, causal, key_padding_lens, S, stream);
+  if (st != ATTN_OK) return st;
+  return attn_merge_states(o_st, m_st, l_st, S, static_cast<long long>(rows), d, O, LSE, stream);
+}
+
+}  // extern "C"

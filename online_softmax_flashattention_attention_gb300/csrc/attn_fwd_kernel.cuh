@@ -60,6 +60,13 @@ struct FwdParams {
   uint32_t* status;        // device status word (bit 0: a wait ran out)
   unsigned long long timeout_ns;
   int fault_block;         // test hook: the K block the producer never loads (-1: none)
+  // partial-state mode only: CTA (unit, split) absorbs key blocks [split * split_blocks,
+  // (split + 1) * split_blocks) and writes the state (m, l, o~) instead of O and LSE
+  int num_splits;          // >= 1
+  int split_blocks;        // key blocks per split, >= 1
+  float* st_o;             // [num_splits, BH, Nq, D] fp32 o~ (unnormalised)
+  float* st_m;             // [num_splits, BH, Nq] running max of the scaled scores (natural log units)
+  float* st_l;             // [num_splits, BH, Nq] running denominator
 };
 
 template <int D>
@@ -100,7 +107,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-template <int D>
+template <int D, bool kStates>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -133,8 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- work unit: heads in order (their K/V stay in L2 while their tiles run);
   //      within a head, causal tiles longest first
   const int nqt = p.num_qtiles;
-  const int bh = blockIdx.x / nqt;
-  int qtile = blockIdx.x % nqt;
+  const int split = kStates ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
+  const int unit = kStates ? static_cast<int>(blockIdx.x / p.num_splits) : static_cast<int>(blockIdx.x);
+  const int bh = unit / nqt;
+  int qtile = unit % nqt;
   if (p.causal) qtile = nqt - 1 - qtile;
   const int b = bh / p.H;
   const int q0 = qtile * kBM;
@@ -146,7 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qlast = min(q0 + kBM - 1, p.Nq - 1);
   const int max_limit = row_key_limit(qlast, kv_len, p.Nq, p.Nk, p.causal);
   const int min_limit = row_key_limit(q0, kv_len, p.Nq, p.Nk, p.causal);
-  const int nblk = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;
+  const int nvis = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;  // key blocks any row of the tile sees
+  // this CTA absorbs key blocks jb0 .. jb0 + nblk - 1 (all of them unless it computes one split)
+  const int jb0 = kStates ? split * p.split_blocks : 0;
+  const int nblk = kStates ? max(0, min(nvis, jb0 + p.split_blocks) - jb0) : nvis;
 
   WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
@@ -195,15 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
           mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
           for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, j * kBN, bh,
-                        pol_kv);
+            tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, (jb0 + j) * kBN,
+                        bh, pol_kv);
         }
         k_issued = j + 1;
         if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) break;
         mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64, j * kBN, bh,
-                      pol_kv);
+          tma_load_3d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64, (jb0 + j) * kBN,
+                      bh, pol_kv);
         v_issued = j + 1;
       }
       // Let the last copies issued land before this warp leaves (in a normal run they were
@@ -293,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s[kBN];
 #pragma unroll
       for (int k = 0; k < kBN; ++k) s[k] = __uint_as_float(sr[k]);
-      const int kb = j * kBN;
+      const int kb = (jb0 + j) * kBN;
       if (kb + kBN > min_limit) {
 #pragma unroll
         for (int k = 0; k < kBN; ++k)
@@ -372,7 +384,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // one decision for all four softmax warps (the named barriers below need all of them)
     const bool give_up = bar_sync_or(1, 128, !ok || *abort_flag != 0u);
-    if (!give_up) {
+    if constexpr (kStates) {
+      // the state of this split, undivided: o~ and l as accumulated, m back in natural-log
+      // units of the scaled scores (m2 = c * max q.k, c = scale * log2 e, so m = m2 * ln 2)
+      if (!give_up) {
+        const bool store = row < p.Nq;
+        const size_t ridx = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + (store ? row : 0);
+        float4* dst = reinterpret_cast<float4*>(p.st_o + ridx * D);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          if (nblk > 0) {  // warp-wide load: every lane takes part, tail rows then skip the store
+            tmem_ld32(tl + C::kColO + q * 32, o);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = 0u;
+          }
+          if (store) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[q * 8 + k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                           __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+          }
+        }
+        if (store) {
+          p.st_m[ridx] = m * 0.69314718055994531f;  // -inf stays -inf for a row that saw no key
+          p.st_l[ridx] = l;
+        }
+      }
+    } else if (!give_up) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint8_t* orow = smem + C::kOffQ + r * 128;
 #pragma unroll

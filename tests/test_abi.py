@@ -65,3 +65,59 @@ def test_empty_problems_are_noops(lib):
         assert pkg.attn_fwd_raw(None, None, None, None, None, B, H, Nq, 16, 64, 0.125, 0, None, None) == 0
     # Nk == 0 still needs the outputs (every row is written as fully masked)
     assert pkg.attn_fwd_raw(None, None, None, None, None, 1, 1, 4, 0, 64, 0.125, 0, None, None) == -1
+
+
+# ---- split-KV entry points: argument checks and workspace sizes (no device needed)
+
+def _states_call(lib, **kw):
+    a = dict(Q=0x10000, K=0x20000, V=0x30000, o=0x40000, m=0x50000, l=0x60000, B=1, H=2, Nq=256, Nk=512, d=128,
+             scale=0.125, causal=0, lens=None, S=2, stream=None)
+    a.update(kw)
+    return lib.attn_fwd_states(a["Q"], a["K"], a["V"], a["o"], a["m"], a["l"], a["B"], a["H"], a["Nq"], a["Nk"],
+                               a["d"], a["scale"], a["causal"], a["lens"], a["S"], a["stream"])
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(S=0), -8), (dict(S=257), -8), (dict(S=-3), -8), (dict(d=96), -3), (dict(l=0), -1), (dict(o=0), -1),
+    (dict(l=0x60004), -4), (dict(o=0x40008), -4), (dict(scale=0.0), -8),
+])
+def test_states_argument_errors(lib, args, status):
+    assert _states_call(lib, **args) == status
+
+
+def _merge_call(lib, **kw):
+    a = dict(o=0x10000, m=0x20000, l=0x30000, S=3, rows=100, d=128, O=0x40000, LSE=0x50000, stream=None)
+    a.update(kw)
+    return lib.attn_merge_states(a["o"], a["m"], a["l"], a["S"], a["rows"], a["d"], a["O"], a["LSE"], a["stream"])
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(d=32), -3), (dict(S=0), -8), (dict(rows=-1), -2), (dict(o=0), -1), (dict(LSE=0), -1),
+    (dict(o=0x10004), -4), (dict(O=0x40002), -4), (dict(m=0x20001), -4),
+])
+def test_merge_argument_errors(lib, args, status):
+    assert _merge_call(lib, **args) == status
+
+
+def test_merge_of_no_rows_is_a_noop(lib):
+    assert _merge_call(lib, rows=0, o=None, m=None, l=None, O=None, LSE=None) == 0
+
+
+def test_splitkv_workspace_bytes(lib):
+    f = lib.attn_splitkv_workspace_bytes
+    rows = 2 * 4 * 300 * 3
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert f(2, 4, 300, 128, 3) == up(rows * 128 * 4) + 2 * up(rows * 4)
+    assert f(2, 4, 300, 64, 3) == up(rows * 64 * 4) + 2 * up(rows * 4)
+    assert f(2, 4, 300, 96, 3) == 0 and f(2, 4, 300, 128, 0) == 0 and f(-1, 4, 300, 128, 2) == 0
+
+
+def test_splitkv_workspace_checks(lib):
+    def call(ws, ws_bytes, S=4):
+        return lib.attn_fwd_splitkv(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, 128, 4096, 128, 0.125, 0,
+                                    None, S, ws, ws_bytes, None)
+    need = lib.attn_splitkv_workspace_bytes(1, 2, 128, 128, 4)
+    assert call(None, need) == -1
+    assert call(0x70008, need) == -4
+    assert call(0x70000, need - 1) == -8
+    assert call(0x70000, need, S=300) == -8
