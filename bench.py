@@ -1,6 +1,7 @@
 """Benchmark of the fused attention forward (one JSON line on stdout, rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+                    [--path fused|splitkv]
 
 A step is one pass of the whole path (one attn_fwd launch) over one batch of the
 workload; the default workload is the causal B=2 H=32 N=8192 d=128 forward, the
@@ -13,12 +14,17 @@ with key padding) per step / device time per step, summed over ranks.
 Under torchrun each rank runs its own copy of the workload (weak scaling, no
 collective on the data path); the barrier and the max-over-ranks time remain.
 
+--path splitkv times the split-KV route instead (attn_fwd_states over the automatic
+split count, then attn_merge_states: two launches per step), the route for shapes
+with few query tiles such as causal_b1h32q128k32768d128.
+
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample
 of the same workload (rows computed one by one), on the same metric.
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -35,11 +41,22 @@ sys.path.insert(0, ROOT)
 METRIC = "attention fwd TFLOP/s (bf16, d=128) and % of GB300 BF16 tensor peak"
 DEFAULT_WORKLOAD = "causal_b2h32n8192d128"
 FALLBACK_PEAK_TFLOPS = 1900.0
-KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh", "attn_api.cu"]
+FALLBACK_PEAK_GBS = 6800.0
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_merge_kernel.cuh"]
 
 
 def algorithmic_flops(B, H, Nq, Nk, d, causal, lens=None) -> float:
-    """4*B*H*Nq*Nk*d, halved for causal; with key padding only valid keys count."""
+    """4*B*H*Nq*Nk*d, halved for causal; with key padding only valid keys count.  For a
+    causal problem with Nq != Nk (bottom-right aligned) the visible pairs are counted
+    exactly: row i sees min(L, i + Nk - Nq + 1) keys."""
+    if causal and Nq != Nk:
+        Ls = [Nk] * B if lens is None else [min(max(int(L), 0), Nk) for L in lens]
+        pairs = 0
+        for L in Ls:
+            lim = min(L, Nk - Nq + 1)          # row 0's limit; it grows by one per row up to L
+            for i in range(Nq):
+                pairs += max(min(L, lim + i), 0)
+        return 4.0 * H * pairs * d
     if lens is not None:
         nk = float(sum(min(max(int(L), 0), Nk) for L in lens))
         f = 4.0 * H * Nq * nk * d
@@ -76,6 +93,24 @@ def load_peaks():
         return float(p["bf16_tflops"]), "measured burst (MEASURED_PEAKS.json bf16_tflops)"
     except (OSError, KeyError, ValueError):
         return FALLBACK_PEAK_TFLOPS, "fallback"
+
+
+def load_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured copy (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_PEAK_GBS, "fallback"
+
+
+def algorithmic_bytes(B, H, Nq, Nk, d, lens=None, splits=0) -> float:
+    """Bytes the kernel must move at least: Q, and K and V of the valid keys, read once;
+    O (bf16) and LSE (fp32) written once -- or, for the partial-state kernel (splits > 0),
+    the states o~ (fp32 d-vector), m and l of every (split, row) written instead."""
+    nk = B * Nk if lens is None else sum(min(max(int(L), 0), Nk) for L in lens)
+    read = 2.0 * H * d * (B * Nq + 2 * nk)
+    write = (2.0 * d + 4) * B * H * Nq if splits == 0 else (4.0 * d + 8) * splits * B * H * Nq
+    return read + write
 
 
 def load_traffic(workload: str):
@@ -254,6 +289,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "splitkv"], default="fused")
     return ap.parse_args()
 
 
@@ -264,12 +300,33 @@ def dist_env():
     return world, rank, local
 
 
-def config_of(w, lens, world):
-    return {"workload": w["name"], "B": w["B"], "H": w["H"], "Nq": w["Nq"], "Nk": w["Nk"], "d": w["d"],
+def roofline_entry(intensity, ridge, tflops, peak, peak_src, kbytes, ms_kernel, hbm_peak, hbm_src, traffic, flops,
+                   kernel):
+    """The dominant kernel against the roof that bounds it: the tensor core when its
+    arithmetic intensity (algorithmic flops / algorithmic bytes) is above the ridge of
+    the measured peaks, HBM bandwidth below it."""
+    common = {"traffic": traffic, "kernel": kernel, "kernel_ms": ms_kernel, "flops_per_launch": flops,
+              "bytes_per_launch": kbytes, "intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
+    if intensity >= ridge:
+        return {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                "peak_source": peak_src, **common}
+    gbs = kbytes / (ms_kernel * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "peak_source": hbm_src, "tflops": tflops, **common}
+
+
+def l2_note(w):
+    mb = (2 * w["B"] * w["H"] * (2 * w["Nq"] + 2 * w["Nk"]) * w["d"] + 4 * w["B"] * w["H"] * w["Nq"]) / 1e6
+    if mb > 129:
+        return f"no flush: inputs and outputs larger than L2 ({mb:.0f} MB per step vs 129 MB L2)"
+    return f"no flush: working set {mb:.1f} MB fits in the 129 MB L2 (repeated steps hit L2)"
+
+
+def config_of(w, lens, world, path="fused", splits=1):
+    return {"workload": w["name"], "path": path if path == "fused" else f"splitkv (S={splits} + merge)", "B": w["B"], "H": w["H"], "Nq": w["Nq"], "Nk": w["Nk"], "d": w["d"],
             "causal": w["causal"], "key_padding": None if lens is None else [int(x) for x in lens],
             "layout": "[B,H,N,d] bf16, O bf16, LSE fp32",
-            "l2": "no flush: inputs and outputs larger than L2 (537 MB per step vs 129 MB L2)"
-            if w["name"] == DEFAULT_WORKLOAD else "no flush",
+            "l2": l2_note(w),
             "parallelism": f"replicas x{world} (each rank its own problem)"}
 
 
@@ -345,8 +402,40 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     flops = algorithmic_flops(B, H, Nq, Nk, d, causal, lens)
 
-    def step():
-        pkg.attn_fwd(Q, K, V, O, LSE, scale=scale, causal=causal, key_padding_lens=lt, stream=stream)
+    lib = pkg.load_library()
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    lens_ptr = None if lt is None else lt.data_ptr()
+    fwd_args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d, scale,
+                int(causal), lens_ptr, sh)
+
+    def check(rc):
+        if rc != 0:
+            raise pkg.AttnError(rc, lib.attn_last_error().decode())
+
+    splits = 1
+    if args.path == "fused":
+        launches_per_step = 1
+
+        def step(evs=None):
+            check(lib.attn_fwd(*fwd_args))
+    else:
+        splits = pkg.splitkv_splits(B, H, Nq, Nk)
+        launches_per_step = 2
+        o_st = torch.empty((splits, B, H, Nq, d), dtype=torch.float32, device=dev)
+        m_st = torch.empty((splits, B, H, Nq), dtype=torch.float32, device=dev)
+        l_st = torch.empty((splits, B, H, Nq), dtype=torch.float32, device=dev)
+        st_args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), o_st.data_ptr(), m_st.data_ptr(), l_st.data_ptr(), B,
+                   H, Nq, Nk, d, scale, int(causal), lens_ptr, splits, sh)
+        mg_args = (o_st.data_ptr(), m_st.data_ptr(), l_st.data_ptr(), splits, B * H * Nq, d, O.data_ptr(),
+                   LSE.data_ptr(), sh)
+
+        def step(evs=None):
+            if evs:
+                evs[0].record(stream)
+            check(lib.attn_fwd_states(*st_args))
+            if evs:
+                evs[1].record(stream)
+            check(lib.attn_merge_states(*mg_args))
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
@@ -362,10 +451,13 @@ def main():
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     sampler.mark("t_start")
+    # split path: events around every states launch give that kernel's own duration
+    kev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)] if args.path == "splitkv" else None)
     ev0.record(stream)
     with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            step()
+        for i in range(args.steps):
+            step(kev[i] if kev else None)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     sampler.mark("t_stop")
@@ -380,11 +472,45 @@ def main():
         ms_total = float(t.item())
     ms_step = ms_total / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
-    per_launch_tflops = flops / (ms_step * 1e-3) / 1e12
+    ms_kernel = ms_step if not kev else sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    per_launch_tflops = flops / (ms_kernel * 1e-3) / 1e12
 
     # ---- end to end through the host-buffer C entry point (pinned host memory)
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and args.path == "splitkv":
+        # the same two C calls, fed from pinned host buffers copied in and out every step
+        Qh, Kh, Vh = (torch.from_numpy(c.view(np.int16)).view(torch.bfloat16).pin_memory()
+                      for c in (x["Q"], x["K"], x["V"]))
+        Oh = torch.empty_like(Qh).pin_memory()
+        Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                Q.copy_(Qh, non_blocking=True)
+                K.copy_(Kh, non_blocking=True)
+                V.copy_(Vh, non_blocking=True)
+                step()
+                Oh.copy_(O, non_blocking=True)
+                Lh.copy_(LSE, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        if pg:
+            pg.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+        if pg:
+            t = torch.tensor([e2e_s], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (Qh.numel() + Kh.numel() + Vh.numel()) * 2,
+               "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4, "ms_per_step": e2e_s * 1e3,
+               "api": "attn_fwd_states + attn_merge_states (C ABI) with pinned host copies inside the timed region"}
+    elif args.e2e_steps > 0:
         def pinned(codes):
             return torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).pin_memory()
 
@@ -411,17 +537,20 @@ def main():
                "api": "attn_fwd_host (C ABI, pinned host buffers, copies inside the timed region)"}
 
     peak, peak_src = load_peaks()
-    traffic = load_traffic(w["name"])
+    hbm_peak, hbm_src = load_hbm_peak()
+    kbytes = algorithmic_bytes(B, H, Nq, Nk, d, lens, 0 if args.path == "fused" else splits)
+    intensity = flops / kbytes
+    ridge = peak * 1e12 / (hbm_peak * 1e9)
+    traffic = load_traffic(w["name"] if args.path == "fused" else w["name"] + ":splitkv")
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": config_of(w, lens, world),
-           "roofline": {"bound": "tensor", "achieved": per_launch_tflops, "peak": peak, "unit": "TFLOP/s",
-                        "frac": per_launch_tflops / peak, "traffic": traffic,
-                        "kernel": f"attn_fwd_kernel<{d}>", "peak_source": peak_src,
-                        "flops_per_launch": flops},
+           "config": config_of(w, lens, world, args.path, splits),
+           "roofline": roofline_entry(intensity, ridge, per_launch_tflops, peak, peak_src, kbytes, ms_kernel,
+                                      hbm_peak, hbm_src, traffic, flops,
+                                      f"attn_fwd_kernel<{d}>" + ("" if args.path == "fused" else " (states)")),
            "e2e": e2e,
-           "gpu_launches": args.steps,
+           "gpu_launches": args.steps * launches_per_step,
            "clocks": clocks,
            "cpu_baseline": cpu}
     if rank == 0:
