@@ -76,6 +76,35 @@ typedef enum {
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                      int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, void* stream);
 
+/* Exponential evaluation modes (attn_options.exp2_mode). */
+enum {
+  ATTN_EXP2_DEFAULT = 0,   /* the library's choice (currently ATTN_EXP2_HARDWARE: measured fastest) */
+  ATTN_EXP2_HARDWARE = 1,  /* every exp2 on the MUFU unit (ex2.approx) */
+  ATTN_EXP2_MIXED = 2      /* in blocks without a masked key, 1 of every 16 pairs of scores takes
+                              a degree-4 polynomial on the FMA pipe (relative error < 3e-6) */
+};
+
+/* Per-call choices for attn_fwd_ex.  Set size = sizeof(attn_options); zero the rest for
+ * the defaults.  (An addition of this library; the pages fix neither choice.) */
+typedef struct attn_options {
+  size_t size;
+  /* Lazy rescale: the running max m is moved (and l, o~ rescaled) only when a block's max
+   * exceeds it by more than this many natural-log units; in between, p = exp(s - m) may
+   * reach exp(threshold).  0 = the pages' rule (rescale whenever the max rises).  The
+   * result is the same in exact arithmetic: softmax is invariant to the reference
+   * ("FlashAttention math", "Safe softmax": any constant m).  Range [0, 20]. */
+  float rescale_threshold;
+  int exp2_mode;           /* ATTN_EXP2_* */
+} attn_options;
+
+/*
+ * attn_fwd_ex -- attn_fwd with options (opts may be NULL: the defaults, identical to
+ * attn_fwd).  Errors: as attn_fwd, plus ATTN_ERR_BAD_ARG for a bad options struct.
+ */
+attn_status attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                        int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
+                        const attn_options* opts, void* stream);
+
 /*
  * attn_fwd_host -- the same operation on HOST buffers (pinned memory recommended).
  * Copies Q, K, V (and key_padding_lens, a host int32[B] or NULL) to the device on

@@ -14,13 +14,21 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn.so")
 
-EXPORTS = ("attn_fwd", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
            "attn_version", "attn_fwd_noalloc", "attn_fwd_states", "attn_merge_states",
            "attn_splitkv_workspace_bytes", "attn_splitkv_splits", "attn_fwd_splitkv")
 
 STATUS_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_NULLPTR", -2: "ATTN_ERR_BAD_SHAPE", -3: "ATTN_ERR_UNSUPPORTED_D",
                 -4: "ATTN_ERR_MISALIGNED", -5: "ATTN_ERR_NO_DEVICE", -6: "ATTN_ERR_LAUNCH", -7: "ATTN_ERR_TIMEOUT",
                 -8: "ATTN_ERR_BAD_ARG"}
+
+
+EXP2_DEFAULT, EXP2_HARDWARE, EXP2_MIXED = 0, 1, 2
+
+
+class AttnOptions(ctypes.Structure):
+    """attn_options of include/attn.h."""
+    _fields_ = [("size", ctypes.c_size_t), ("rescale_threshold", ctypes.c_float), ("exp2_mode", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -52,6 +60,8 @@ def load_library():
         lib.attn_last_error.restype = ctypes.c_char_p
         lib.attn_version.argtypes = []
         lib.attn_version.restype = i
+        lib.attn_fwd_ex.argtypes = sig[:-1] + [ctypes.POINTER(AttnOptions), vp]
+        lib.attn_fwd_ex.restype = i
         lib.attn_fwd_states.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
         lib.attn_fwd_states.restype = i
         lib.attn_merge_states.argtypes = [vp, vp, vp, i, ctypes.c_longlong, i, vp, vp, vp]
@@ -117,12 +127,14 @@ def _outputs(Q, O, LSE):
     return O, LSE
 
 
-def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding_lens=None, stream=None):
+def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding_lens=None, stream=None,
+             rescale_threshold=0.0, exp2_mode=EXP2_DEFAULT):
     """O, LSE = softmax(scale * Q K^T + mask) V and its row logsumexp, on the GPU.
 
     Q [B,H,Nq,d], K/V [B,H,Nk,d]: contiguous bf16 CUDA tensors.  O (bf16) and LSE
     (fp32 [B,H,Nq]) are allocated when not given.  key_padding_lens: int32 CUDA
     tensor [B] or None.  Enqueued on ``stream`` (default: torch's current stream).
+    rescale_threshold / exp2_mode: the attn_options of attn_fwd_ex (defaults: attn_fwd).
     """
     import torch
     B, H, Nq, d = Q.shape
@@ -147,8 +159,14 @@ def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding
         if key_padding_lens.dtype != torch.int32 or not key_padding_lens.is_cuda or key_padding_lens.numel() != B:
             raise ValueError("key_padding_lens must be an int32 CUDA tensor [B]")
         lens_ptr = key_padding_lens.data_ptr()
-    rc = attn_fwd_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d,
-                      float(scale), causal, lens_ptr, _stream_handle(stream))
+    if rescale_threshold == 0.0 and exp2_mode == EXP2_DEFAULT:
+        rc = attn_fwd_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d,
+                          float(scale), causal, lens_ptr, _stream_handle(stream))
+    else:
+        opts = AttnOptions(ctypes.sizeof(AttnOptions), float(rescale_threshold), int(exp2_mode))
+        rc = load_library().attn_fwd_ex(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H,
+                                        Nq, Nk, d, float(scale), int(causal), lens_ptr, ctypes.byref(opts),
+                                        _stream_handle(stream))
     _check(rc)
     return O, LSE
 

@@ -34,7 +34,6 @@ attn_status fail(attn_status st, const char* fmt, ...) {
 
 std::mutex g_mu;
 uint32_t* g_status[kMaxDevices] = {};
-bool g_attr_set[kMaxDevices][4] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -136,19 +135,38 @@ struct StateOut {
   int num_splits = 1;
 };
 
-template <int D, bool kStates>
-attn_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
-                   float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
-                   const StateOut& so = StateOut{}) {
+// How many of every 16 score pairs of an unmasked block take the polynomial exponential
+// (exp2_poly2) in ATTN_EXP2_MIXED mode, per head dimension: of the splits measured on
+// GB300 (1 to 5 of 16) the least slow; every split was slower than ex2.approx alone, so
+// the default mode is ATTN_EXP2_HARDWARE.  The macros let a build try other splits.
+#ifndef ATTN_SOFT_PAIRS_D128
+#define ATTN_SOFT_PAIRS_D128 1
+#endif
+#ifndef ATTN_SOFT_PAIRS_D64
+#define ATTN_SOFT_PAIRS_D64 1
+#endif
+template <int D>
+constexpr int kDefaultSoftPairs = (D == 128) ? ATTN_SOFT_PAIRS_D128 : ATTN_SOFT_PAIRS_D64;
+
+// Per-call choices the options struct carries, resolved for the kernel.
+struct Variant {
+  float tau_log2 = 0.f;  // rescale threshold in log2 units
+  bool soft = false;     // mixed exponentials (kDefaultSoftPairs) or ex2.approx only (default)
+};
+
+template <int D, bool kStates, int kSoft>
+attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                       int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
+                       uint32_t* status, const StateOut& so, const Variant& var) {
   using C = attn::FwdCfg<D>;
-  auto kernel = attn::attn_fwd_kernel<D, kStates>;
-  const int di = ((D == 128) ? 1 : 0) + (kStates ? 2 : 0);
+  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft>;
+  static bool attr_set[kMaxDevices] = {};  // one flag per device for this instantiation
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_attr_set[dev][di]) {
+    if (!attr_set[dev]) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
       if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      g_attr_set[dev][di] = true;
+      attr_set[dev] = true;
     }
   }
   const int BH = B * H;
@@ -180,6 +198,7 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   p.status = status;
   p.timeout_ns = wait_limit_ns();
   p.fault_block = fault_block();
+  p.tau = var.tau_log2;
   const int nkb = (Nk + attn::kBN - 1) / attn::kBN;
   p.num_splits = kStates ? so.num_splits : 1;
   p.split_blocks = kStates ? std::max(1, (nkb + so.num_splits - 1) / so.num_splits) : std::max(1, nkb);
@@ -191,6 +210,33 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+template <int D, bool kStates>
+attn_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
+                   float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
+                   const StateOut& so = StateOut{}, const Variant& var = Variant{}) {
+  if (var.soft)
+    return launch_one<D, kStates, kDefaultSoftPairs<D>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream,
+                                                        dev, status, so, var);
+  return launch_one<D, kStates, 0>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, so,
+                                   var);
+}
+
+// Options -> kernel variant; NULL means the defaults.
+attn_status resolve_options(const attn_options* opts, Variant* var) {
+  *var = Variant{};
+  if (!opts) return ATTN_OK;
+  if (opts->size < sizeof(attn_options))
+    return fail(ATTN_ERR_BAD_ARG, "attn_options.size=%zu; expected %zu", opts->size, sizeof(attn_options));
+  const float t = opts->rescale_threshold;
+  if (!std::isfinite(t) || t < 0.f || t > 20.f)
+    return fail(ATTN_ERR_BAD_ARG, "rescale_threshold=%g; must be in [0, 20]", static_cast<double>(t));
+  if (opts->exp2_mode < ATTN_EXP2_DEFAULT || opts->exp2_mode > ATTN_EXP2_MIXED)
+    return fail(ATTN_ERR_BAD_ARG, "exp2_mode=%d", opts->exp2_mode);
+  var->tau_log2 = static_cast<float>(static_cast<double>(t) * 1.4426950408889634);
+  var->soft = opts->exp2_mode == ATTN_EXP2_MIXED;
   return ATTN_OK;
 }
 
@@ -212,6 +258,27 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
   if (d == 128)
     return launch<128, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
   return launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status);
+}
+
+attn_status attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                        int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
+                        const attn_options* opts, void* stream) {
+  g_err[0] = '\0';
+  Variant var;
+  attn_status st = resolve_options(opts, &var);
+  if (st != ATTN_OK) return st;
+  if ((st = check_args(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale)) != ATTN_OK) return st;
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  int dev;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  uint32_t* status = nullptr;
+  if ((st = setup(dev, &status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    return launch<128, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
+                              StateOut{}, var);
+  return launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
+                           StateOut{}, var);
 }
 
 attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,

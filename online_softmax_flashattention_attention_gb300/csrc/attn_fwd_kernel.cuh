@@ -36,7 +36,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
+#include "exp2_poly.cuh"
 #include "ptx.cuh"
 
 namespace attn {
@@ -60,6 +62,7 @@ struct FwdParams {
   uint32_t* status;        // device status word (bit 0: a wait ran out)
   unsigned long long timeout_ns;
   int fault_block;         // test hook: the K block the producer never loads (-1: none)
+  float tau;               // rescale threshold, log2 units: 0 = rescale whenever the max rises
   // partial-state mode only: CTA (unit, split) absorbs key blocks [split * split_blocks,
   // (split + 1) * split_blocks) and writes the state (m, l, o~) instead of O and LSE
   int num_splits;          // >= 1
@@ -101,13 +104,39 @@ __device__ __forceinline__ int row_key_limit(int row, int kv_len, int Nq, int Nk
   return lim < kv_len ? static_cast<int>(lim < 0 ? 0 : lim) : kv_len;
 }
 
+// 2^x for two values on the FMA and ALU pipes instead of the MUFU unit.  Range reduction
+// after Cody and Waite: j = rint(x) by adding and subtracting 1.5 * 2^23, f = x - j in
+// [-1/2, 1/2], 2^f by the degree-4 polynomial of exp2_poly.cuh (relative error
+// kExp2PolyMaxRelError), then j added to the exponent field.  Arguments below -125 are
+// clamped to -125, so j >= -125 and the exponent field stays >= 1 (2^f >= 2^-1/2 has a
+// field of 126): no wrap into the sign bit.  A clamped value is at most 2^-124.5, which
+// is negligible next to l >= 1.  -inf is clamped too, so masked scores must not come here.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 shifter = make_float2(12582912.f, 12582912.f);
+  const float2 t = __fadd2_rn(x, shifter);                            // 1.5 * 2^23 + rint(x)
+  const float2 nj = __ffma2_rn(t, make_float2(-1.f, -1.f), shifter);  // -rint(x), exact
+  const float2 f = __fadd2_rn(x, nj);
+  float2 r = __ffma2_rn(make_float2(kExp2C4, kExp2C4), f, make_float2(kExp2C3, kExp2C3));
+  r = __ffma2_rn(r, f, make_float2(kExp2C2, kExp2C2));
+  r = __ffma2_rn(r, f, make_float2(kExp2C1, kExp2C1));
+  r = __ffma2_rn(r, f, make_float2(kExp2C0, kExp2C0));
+  // the low bits of t hold rint(x) in two's complement: shifted into the exponent field
+  r.x = __uint_as_float(__float_as_uint(r.x) + (__float_as_uint(t.x) << 23));
+  r.y = __uint_as_float(__float_as_uint(r.y) + (__float_as_uint(t.y) << 23));
+  return r;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-template <int D, bool kStates>
+// kSoftPairs: of every 16 pairs of scores in a block with no masked key, this many take
+// their exponential from exp2_poly2 instead of ex2.approx, to relieve the MUFU unit.
+template <int D, bool kStates, int kSoftPairs>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -321,29 +350,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmax3(a[c8], s[k + 2 * c8], s[k + 2 * c8 + 1]);
       }
       const float mx = fmaxf(fmaxf(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5])), fmaxf(a[6], a[7]));
-      const float m_new = fmaxf(m, mx * c);
+      // the reference moves when the block max passes it by more than tau (tau = 0: whenever
+      // the max rises, the pages' rule; a row that has seen no visible key stays at -inf)
+      const float mb = mx * c;
+      const float m_new = (mb > m + p.tau) ? mb : m;
       const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = ex2_approx(m - m_ref);
       // p = exp2(c*s - m_ref), summed in fp32, packed to bf16 and stored 32 keys at a time
       const float2 c2 = make_float2(c, c);
       const float2 nm2 = make_float2(-m_ref, -m_ref);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      auto exp_block = [&](auto soft_tag) {
+        constexpr bool kSoft = decltype(soft_tag)::value;
 #pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) {
-        uint32_t pk[16];
+        for (int q = 0; q < kBN / 32; ++q) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float2 x = __ffma2_rn(make_float2(s[q * 32 + 2 * k], s[q * 32 + 2 * k + 1]), c2, nm2);
-          x.x = ex2_approx(x.x);
-          x.y = ex2_approx(x.y);
-          if (k & 1)
-            acc1 = __fadd2_rn(acc1, x);
-          else
-            acc0 = __fadd2_rn(acc0, x);
-          pk[k] = pack_bf16x2(x.x, x.y);
+          for (int k = 0; k < 16; ++k) {
+            float2 x = __ffma2_rn(make_float2(s[q * 32 + 2 * k], s[q * 32 + 2 * k + 1]), c2, nm2);
+            if (kSoft && (k * kSoftPairs) % 16 < kSoftPairs) {
+              x = exp2_poly2(x);
+            } else {
+              x.x = ex2_approx(x.x);
+              x.y = ex2_approx(x.y);
+            }
+            if (k & 1)
+              acc1 = __fadd2_rn(acc1, x);
+            else
+              acc0 = __fadd2_rn(acc0, x);
+            pk[k] = pack_bf16x2(x.x, x.y);
+          }
+          tmem_st16(tl + colS + q * 16, pk);
         }
-        tmem_st16(tl + colS + q * 16, pk);
-      }
+      };
+      // blocks with a masked key (-inf scores) keep every exponential on ex2.approx
+      if (kSoftPairs > 0 && kb + kBN <= min_limit)
+        exp_block(std::true_type{});
+      else
+        exp_block(std::false_type{});
       const float2 acc = __fadd2_rn(acc0, acc1);
       l = l * alpha + (acc.x + acc.y);
       m = m_new;

@@ -9,9 +9,12 @@
 // saw no visible key (every m_s = -inf) gets O = 0, LSE = -inf.
 //
 // The merge reads S * (4 d + 8) bytes and writes 2 d + 4 bytes per row: it is bound by
-// HBM bandwidth.  One warp owns one row; lane t holds columns [t * d/32, (t+1) * d/32),
-// so each state's o~ row is one coalesced 256- or 512-byte read.  Rows are spread over
-// a grid sized to the SM count (grid-stride loop).
+// memory bandwidth once enough loads are in flight.  One warp owns one row; lane t holds
+// columns [t * d/32, (t+1) * d/32), so each state's o~ row is one coalesced 256- or
+// 512-byte read.  States are taken eight at a time: all their loads are issued before
+// any arithmetic, and the chunks fold into a running (M, L, o~) with the same identity,
+// so a row costs one round trip to memory per eight states.  Rows are spread over a grid
+// sized to the SM count (grid-stride loop).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -37,49 +40,66 @@ struct MergeParams {
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const MergeParams p) {
-  constexpr int kPer = D / 32;  // columns per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int kPer = D / 32;    // columns per lane: 4 (d = 128) or 2 (d = 64)
+  constexpr int kChunk = 8;       // states loaded together: one round of independent loads
   constexpr float kLog2e = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
   for (long long row = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
        row < p.rows; row += warps) {
-    // the common reference: the largest running max over the states
-    float mx = -INFINITY;
-    for (int s = lane; s < p.S; s += 32) mx = fmaxf(mx, __ldg(p.st_m + static_cast<long long>(s) * p.rows + row));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float ref = (mx == -INFINITY) ? 0.f : mx;
-    // l = sum_s exp(m_s - m) l_s  (an empty state has m_s = -inf, factor 0)
-    float lsum = 0.f;
-    for (int s = lane; s < p.S; s += 32) {
-      const long long i = static_cast<long long>(s) * p.rows + row;
-      lsum += ex2_approx((__ldg(p.st_m + i) - ref) * kLog2e) * __ldg(p.st_l + i);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    // o~ = sum_s exp(m_s - m) o~_s, this lane's columns
+    // running merge over chunks of states: (M, L, acc) is the state of the states seen
+    float M = -INFINITY, L = 0.f;
     float acc[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < p.S; ++s) {
-      const long long i = static_cast<long long>(s) * p.rows + row;
-      const float w = ex2_approx((__ldg(p.st_m + i) - ref) * kLog2e);
-      const float* src = p.st_o + i * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
-      } else {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
+    for (int s0 = 0; s0 < p.S; s0 += kChunk) {
+      float ms[kChunk], ls[kChunk], os[kChunk][kPer];
+      // every load of the chunk first (m and l are the same address for all lanes)
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const int s = s0 + c;
+        ms[c] = -INFINITY;
+        ls[c] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) os[c][k] = 0.f;
+        if (s < p.S) {
+          const long long i = static_cast<long long>(s) * p.rows + row;
+          ms[c] = __ldg(p.st_m + i);
+          ls[c] = __ldg(p.st_l + i);
+          const float* src = p.st_o + i * D + lane * kPer;
+          if constexpr (kPer == 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+            os[c][0] = v.x;
+            os[c][1] = v.y;
+            os[c][2] = v.z;
+            os[c][3] = v.w;
+          } else {
+            const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+            os[c][0] = v.x;
+            os[c][1] = v.y;
+          }
+        }
       }
+      // new common reference, then every state (and the running one) rescaled to it
+      float mc = M;
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) mc = fmaxf(mc, ms[c]);
+      const float ref = (mc == -INFINITY) ? 0.f : mc;
+      const float a = ex2_approx((M - ref) * kLog2e);  // 0 while nothing was seen
+      L *= a;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) acc[k] *= a;
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const float w = ex2_approx((ms[c] - ref) * kLog2e);  // 0 for an empty state
+        L = fmaf(w, ls[c], L);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) acc[k] = fmaf(w, os[c][k], acc[k]);
+      }
+      M = mc;
     }
     // the single final division
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat16* dst = p.O + row * D + lane * kPer;
     if constexpr (kPer == 4) {
       uint2 packed;
@@ -89,7 +109,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const MergePa
     } else {
       *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
-    if (lane == 0) p.lse[row] = lsum > 0.f ? mx + logf(lsum) : -INFINITY;
+    if (lane == 0) p.lse[row] = L > 0.f ? M + logf(L) : -INFINITY;
   }
 }
 

@@ -121,3 +121,58 @@ def test_splitkv_workspace_checks(lib):
     assert call(0x70008, need) == -4
     assert call(0x70000, need - 1) == -8
     assert call(0x70000, need, S=300) == -8
+
+
+def test_options_struct_checks(lib):
+    def call(**kw):
+        o = pkg.AttnOptions(ctypes.sizeof(pkg.AttnOptions), kw.get("tau", 0.0), kw.get("mode", 0))
+        if "size" in kw:
+            o.size = kw["size"]
+        return lib.attn_fwd_ex(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, 256, 256, 64, 0.125, 0, None,
+                               ctypes.byref(o), None)
+    assert call(size=4) == -8
+    assert call(tau=-1.0) == -8
+    assert call(tau=21.0) == -8
+    assert call(tau=float("nan")) == -8
+    assert call(mode=3) == -8
+    assert call(mode=-1) == -8
+    assert ctypes.sizeof(pkg.AttnOptions) == 16
+
+
+def test_exp2_polynomial_bound():
+    """The committed coefficients reproduce the generator's stated bound, evaluated in
+    float32 the way the kernel does (Horner, one rounding per fused multiply-add); with
+    the kernel's clamp, range reduction and exponent-field scaling (bit for bit, in
+    wrapping 32-bit integers) the bound holds for 2^x on [-125, 29] and every argument
+    below the clamp gives a finite value no larger than 2^-124."""
+    import importlib.util
+    import numpy as np
+    path = os.path.join(ROOT, "online_softmax_flashattention_attention_gb300", "csrc")
+    spec = importlib.util.spec_from_file_location("gen_exp2_poly", os.path.join(path, "gen_exp2_poly.py"))
+    g = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(g)
+    text = open(os.path.join(path, "exp2_poly.cuh")).read()
+    c = np.array([float(re.search(rf"kExp2C{k} = ([0-9.e+-]+)f;", text).group(1)) for k in range(5)], np.float32)
+    bound = float(re.search(r"kExp2PolyMaxRelError = ([0-9.e+-]+)f;", text).group(1))
+    assert bound < 3e-6
+    assert g.max_rel_error(c) <= bound * 1.001
+    kernel = open(os.path.join(path, "attn_fwd_kernel.cuh")).read()
+    lo = float(re.search(r"x\.x = fmaxf\(x\.x, (-[0-9.]+)f\);", kernel).group(1))
+    assert lo == -125.0
+
+    def kernel_exp2(x):
+        x = np.maximum(x.astype(np.float32), np.float32(lo))
+        t = (x + np.float32(12582912.0)).astype(np.float32)
+        nj = (np.float32(12582912.0) - t).astype(np.float32)       # exact
+        f = (x + nj).astype(np.float32)
+        assert np.all(np.abs(f) <= 0.5)
+        p = g.horner_f32(c, f)
+        bits = (p.view(np.uint32).astype(np.uint64) + (t.view(np.uint32).astype(np.uint64) << np.uint64(23)))
+        return (bits & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.float32)
+
+    x = np.linspace(-125.0, 29.0, 2_000_001).astype(np.float32)
+    r = kernel_exp2(x).astype(np.float64)
+    assert np.abs(r / np.exp2(x.astype(np.float64)) - 1.0).max() <= bound * 1.001
+    below = np.concatenate([np.linspace(-1e4, -125.0, 100_001), [-np.inf]]).astype(np.float32)
+    rb = kernel_exp2(below)
+    assert np.all(np.isfinite(rb)) and np.all(rb >= 0) and np.all(rb <= 2.0 ** -124)
