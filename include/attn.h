@@ -106,6 +106,42 @@ attn_status attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, fl
                         const attn_options* opts, void* stream);
 
 /*
+ * attn_fwd_strided -- attn_fwd over tensors with any (batch, head, row) strides, e.g.
+ * the [B, N, H, d] ("BSHD") layout: strides {N*H*d, d, H*d}.  (The pages fix no layout;
+ * an addition of this library.)
+ *   q_strides, k_strides, v_strides, o_strides: host int64[3] each, the element strides
+ *   of the batch, head and row dimensions; element (b, h, i, x) of Q is at
+ *   Q + b*q_strides[0] + h*q_strides[1] + i*q_strides[2] + x (d is contiguous).
+ *   Every stride must be a positive multiple of 8 elements (16 bytes, for TMA) below
+ *   2^38; the rows of O must not overlap.  LSE stays contiguous [B, H, Nq].
+ *   Everything else as attn_fwd.  Errors: as attn_fwd, plus ATTN_ERR_BAD_ARG for a bad
+ *   stride and ATTN_ERR_NULLPTR for a NULL stride array.
+ */
+attn_status attn_fwd_strided(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                             int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
+                             const int64_t* q_strides, const int64_t* k_strides, const int64_t* v_strides,
+                             const int64_t* o_strides, void* stream);
+
+/*
+ * attn_fwd_varlen -- attention over B packed sequences of different lengths (an addition
+ * of this library; the pages treat one sequence).
+ *   Q, O  device bf16 [total_q, H, d]: sequence b is rows cu_seqlens_q[b] ..
+ *         cu_seqlens_q[b+1] - 1.  K, V device bf16 [total_k, H, d], rows cu_seqlens_k[b] ..
+ *   cu_seqlens_q, cu_seqlens_k  device int32[B + 1], non-decreasing from 0 to total_q /
+ *         total_k (values are clamped to [0, total] on the device, so a bad array cannot
+ *         make the kernel write outside O and LSE).
+ *   max_seqlen_q  >= the longest query sequence (the grid covers that many rows; longer
+ *         sequences are left partly unwritten).
+ *   LSE   device fp32 [H, total_q].
+ *   Masks per sequence: query i of sequence b (Nq_b rows, Nk_b keys) sees key j iff
+ *   j < Nk_b and, when causal, j <= i + (Nk_b - Nq_b).  A sequence with no keys gets O = 0
+ *   and LSE = -inf.  Asynchronous; timeouts through attn_status_sync.
+ */
+attn_status attn_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int H, int max_seqlen_q,
+                            int total_q, int total_k, int d, float scale, int causal, void* stream);
+
+/*
  * attn_fwd_host -- the same operation on HOST buffers (pinned memory recommended).
  * Copies Q, K, V (and key_padding_lens, a host int32[B] or NULL) to the device on
  * `stream`, runs attn_fwd, copies O and LSE back and synchronises the stream before it

@@ -14,7 +14,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn.so")
 
-EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_strided", "attn_fwd_varlen", "attn_fwd_host", "attn_release_workspace", "attn_status_sync", "attn_last_error",
            "attn_version", "attn_fwd_noalloc", "attn_fwd_states", "attn_merge_states",
            "attn_splitkv_workspace_bytes", "attn_splitkv_splits", "attn_fwd_splitkv")
 
@@ -62,6 +62,11 @@ def load_library():
         lib.attn_version.restype = i
         lib.attn_fwd_ex.argtypes = sig[:-1] + [ctypes.POINTER(AttnOptions), vp]
         lib.attn_fwd_ex.restype = i
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.attn_fwd_strided.argtypes = sig[:-1] + [i64p, i64p, i64p, i64p, vp]
+        lib.attn_fwd_strided.restype = i
+        lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+        lib.attn_fwd_varlen.restype = i
         lib.attn_fwd_states.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
         lib.attn_fwd_states.restype = i
         lib.attn_merge_states.argtypes = [vp, vp, vp, i, ctypes.c_longlong, i, vp, vp, vp]
@@ -271,5 +276,67 @@ def attn_fwd_splitkv(Q, K, V, O=None, LSE=None, *, num_splits=0, workspace=None,
     rc = load_library().attn_fwd_splitkv(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H,
                                          Nq, Nk, d, float(scale), int(causal), lens_ptr, S, ws_ptr, ws_bytes,
                                          _stream_handle(stream))
+    _check(rc)
+    return O, LSE
+
+
+# --- other layouts -------------------------------------------------------------
+
+def attn_fwd_strided(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding_lens=None, stream=None):
+    """attn_fwd on 4-D bf16 CUDA tensors viewed as [B, H, N, d] with any strides whose last
+    dimension is contiguous (e.g. ``x.transpose(1, 2)`` of a [B, N, H, d] tensor).  O (same
+    strides as a new tensor shaped like Q's view when not given) and LSE [B, H, Nq]."""
+    import torch
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(3) != 1:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor with a contiguous last dimension")
+    if K.shape != (B, H, Nk, d) or V.shape != (B, H, Nk, d):
+        raise ValueError("K and V must be [B, H, Nk, d] with Q's B, H and d")
+    if O is None:
+        O = torch.empty((B, Nq, H, d), dtype=torch.bfloat16, device=Q.device).transpose(1, 2)
+    if LSE is None:
+        LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=Q.device)
+    if O.shape != Q.shape or O.dtype != torch.bfloat16 or O.stride(3) != 1:
+        raise ValueError("O must be bf16 shaped like Q with a contiguous last dimension")
+    lens_ptr = None
+    if key_padding_lens is not None:
+        lens_ptr = key_padding_lens.data_ptr()
+
+    def st(t):
+        return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+    rc = load_library().attn_fwd_strided(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H,
+                                         Nq, Nk, d, float(scale), int(causal), lens_ptr, st(Q), st(K), st(V), st(O),
+                                         _stream_handle(stream))
+    _check(rc)
+    return O, LSE
+
+
+def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, O=None, LSE=None, *, scale=None, causal=False,
+                    stream=None):
+    """Packed sequences: Q [total_q, H, d], K/V [total_k, H, d] contiguous bf16 CUDA tensors,
+    cu_seqlens_q / cu_seqlens_k int32 CUDA tensors [B + 1].  Returns O [total_q, H, d] and
+    LSE [H, total_q]."""
+    import torch
+    total_q, H, d = Q.shape
+    total_k = K.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None:
+        LSE = torch.empty((H, total_q), dtype=torch.float32, device=Q.device)
+    rc = load_library().attn_fwd_varlen(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(),
+                                        cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, H, int(max_seqlen_q),
+                                        total_q, total_k, d, float(scale), int(causal), _stream_handle(stream))
     _check(rc)
     return O, LSE

@@ -76,13 +76,44 @@ attn_status setup(int dev, uint32_t** status) {
   return ATTN_OK;
 }
 
-// 3-D map over a [BH, N, d] bf16 tensor: dims (d, N, BH), box (64, 128, 1), 128-byte swizzle.
-attn_status make_map(CUtensorMap* map, const void* ptr, int BH, int N, int d) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+// Where the four tensors live.  Each is seen through a 4-D map (d, rows, heads,
+// batches) with element strides (batch, head, row); d is contiguous.  Packed sequences
+// use one batch and the per-sequence row offsets cu_q / cu_k.
+struct Geometry {
+  long long qs[3], ks[3], vs[3], os[3];  // element strides: batch, head, row
+  long long q_rows = 0, k_rows = 0;      // rows of the maps
+  int map_b = 1;                         // batches of the maps
+  int grid_q = 0;                        // query rows the grid covers (longest sequence)
+  const int32_t* cu_q = nullptr;
+  const int32_t* cu_k = nullptr;
+};
+
+Geometry dense_geometry(int B, int H, int Nq, int Nk, int d) {
+  Geometry g;
+  const long long qb = static_cast<long long>(H) * Nq * d, kb = static_cast<long long>(H) * Nk * d;
+  const long long q[3] = {qb, static_cast<long long>(Nq) * d, d};
+  const long long k[3] = {kb, static_cast<long long>(Nk) * d, d};
+  for (int i = 0; i < 3; ++i) {
+    g.qs[i] = g.os[i] = q[i];
+    g.ks[i] = g.vs[i] = k[i];
+  }
+  g.q_rows = Nq;
+  g.k_rows = Nk;
+  g.map_b = B;
+  g.grid_q = Nq;
+  return g;
+}
+
+// 4-D map (d, rows, H, B) over bf16 with element strides (batch, head, row), box
+// (64, 128, 1, 1), 128-byte swizzle; rows past `rows` read as zero and are not stored.
+attn_status make_map(CUtensorMap* map, const void* ptr, int d, long long rows, int H, int B, const long long* st) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                           static_cast<cuuint64_t>(st[0]) * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(ATTN_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -157,7 +188,7 @@ struct Variant {
 template <int D, bool kStates, int kSoft>
 attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                        int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
-                       uint32_t* status, const StateOut& so, const Variant& var) {
+                       uint32_t* status, const StateOut& so, const Variant& var, const Geometry& geo) {
   using C = attn::FwdCfg<D>;
   auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft>;
   static bool attr_set[kMaxDevices] = {};  // one flag per device for this instantiation
@@ -172,15 +203,15 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   const int BH = B * H;
   CUtensorMap mq, mk, mv, mo;
   attn_status st;
-  if ((st = make_map(&mq, Q, BH, Nq, D)) != ATTN_OK) return st;
+  if ((st = make_map(&mq, Q, D, geo.q_rows, H, geo.map_b, geo.qs)) != ATTN_OK) return st;
   if (kStates) {
     mo = mq;  // never used: the partial-state epilogue stores with plain writes
-  } else if ((st = make_map(&mo, O, BH, Nq, D)) != ATTN_OK) {
+  } else if ((st = make_map(&mo, O, D, geo.q_rows, H, geo.map_b, geo.os)) != ATTN_OK) {
     return st;
   }
-  if (Nk > 0) {
-    if ((st = make_map(&mk, K, BH, Nk, D)) != ATTN_OK) return st;
-    if ((st = make_map(&mv, V, BH, Nk, D)) != ATTN_OK) return st;
+  if (geo.k_rows > 0) {
+    if ((st = make_map(&mk, K, D, geo.k_rows, H, geo.map_b, geo.ks)) != ATTN_OK) return st;
+    if ((st = make_map(&mv, V, D, geo.k_rows, H, geo.map_b, geo.vs)) != ATTN_OK) return st;
   } else {  // never read: every row is fully masked
     mk = mq;
     mv = mq;
@@ -190,7 +221,7 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   p.H = H;
   p.Nq = Nq;
   p.Nk = Nk;
-  p.num_qtiles = (Nq + attn::kBM - 1) / attn::kBM;
+  p.num_qtiles = (geo.grid_q + attn::kBM - 1) / attn::kBM;
   p.causal = causal ? 1 : 0;
   p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.lens = lens;
@@ -205,6 +236,11 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   p.st_o = so.o;
   p.st_m = so.m;
   p.st_l = so.l;
+  p.cu_q = geo.cu_q;
+  p.cu_k = geo.cu_k;
+  p.total_q = static_cast<int>(geo.q_rows);
+  p.total_k = static_cast<int>(geo.k_rows);
+  p.o_packed = static_cast<__nv_bfloat16*>(O);
   const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH) *
                         static_cast<unsigned>(p.num_splits);
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
@@ -216,12 +252,13 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
 template <int D, bool kStates>
 attn_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
                    float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
-                   const StateOut& so = StateOut{}, const Variant& var = Variant{}) {
+                   const StateOut& so = StateOut{}, const Variant& var = Variant{}, const Geometry* geo = nullptr) {
+  const Geometry g = geo ? *geo : dense_geometry(B, H, Nq, Nk, D);
   if (var.soft)
     return launch_one<D, kStates, kDefaultSoftPairs<D>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream,
-                                                        dev, status, so, var);
-  return launch_one<D, kStates, 0>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, so,
-                                   var);
+                                                        dev, status, so, var, g);
+  return launch_one<D, kStates, 0>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, so, var,
+                                   g);
 }
 
 // Options -> kernel variant; NULL means the defaults.
@@ -279,6 +316,84 @@ attn_status attn_fwd_ex(const void* Q, const void* K, const void* V, void* O, fl
                               StateOut{}, var);
   return launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
                            StateOut{}, var);
+}
+
+attn_status attn_fwd_strided(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                             int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,
+                             const int64_t* q_strides, const int64_t* k_strides, const int64_t* v_strides,
+                             const int64_t* o_strides, void* stream) {
+  g_err[0] = '\0';
+  attn_status st = check_args(Q, K, V, O, LSE, B, H, Nq, Nk, d, scale);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * H == 0 || Nq == 0) return ATTN_OK;
+  if (!q_strides || !k_strides || !v_strides || !o_strides) return fail(ATTN_ERR_NULLPTR, "stride arrays must not be NULL");
+  Geometry g = dense_geometry(B, H, Nq, Nk, d);
+  const int64_t* in[4] = {q_strides, k_strides, v_strides, o_strides};
+  long long* out[4] = {g.qs, g.ks, g.vs, g.os};
+  for (int t = 0; t < 4; ++t)
+    for (int i = 0; i < 3; ++i) {
+      const int64_t v = in[t][i];
+      if (v <= 0 || (v & 7) != 0 || v >= (1ll << 38))
+        return fail(ATTN_ERR_BAD_ARG, "stride %d of tensor %d is %lld; strides must be positive multiples of 8 "
+                    "elements (16 bytes) below 2^38", i, t, static_cast<long long>(v));
+      out[t][i] = v;
+    }
+  int dev;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  uint32_t* status = nullptr;
+  if ((st = setup(dev, &status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    return launch<128, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
+                              StateOut{}, Variant{}, &g);
+  return launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, status,
+                           StateOut{}, Variant{}, &g);
+}
+
+attn_status attn_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B, int H, int max_seqlen_q,
+                            int total_q, int total_k, int d, float scale, int causal, void* stream) {
+  g_err[0] = '\0';
+  if (B < 0 || H < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0)
+    return fail(ATTN_ERR_BAD_SHAPE, "negative size (B=%d H=%d max_seqlen_q=%d total_q=%d total_k=%d)", B, H,
+                max_seqlen_q, total_q, total_k);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED_D, "d=%d; supported: 64, 128", d);
+  if (!std::isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_BAD_ARG, "scale must be finite and > 0");
+  const long long tiles = static_cast<long long>(B) * H * ((max_seqlen_q + attn::kBM - 1) / attn::kBM);
+  if (tiles > INT32_MAX || static_cast<long long>(total_q) * H * d > (1ll << 40))
+    return fail(ATTN_ERR_BAD_SHAPE, "problem too large");
+  if (static_cast<long long>(B) * H == 0 || max_seqlen_q == 0 || total_q == 0) return ATTN_OK;
+  if (!Q || !O || !LSE || !cu_seqlens_q || !cu_seqlens_k)
+    return fail(ATTN_ERR_NULLPTR, "Q, O, LSE and the cu_seqlens arrays must not be NULL");
+  if (total_k > 0 && (!K || !V)) return fail(ATTN_ERR_NULLPTR, "K and V must not be NULL when total_k > 0");
+  if (misaligned(Q) || misaligned(O) || misaligned(LSE) || (total_k > 0 && (misaligned(K) || misaligned(V))))
+    return fail(ATTN_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  Geometry g;
+  const long long row = static_cast<long long>(H) * d;  // packed [total, H, d]
+  const long long q[3] = {static_cast<long long>(total_q) * row, d, row};
+  const long long k[3] = {static_cast<long long>(total_k > 0 ? total_k : 1) * row, d, row};
+  for (int i = 0; i < 3; ++i) {
+    g.qs[i] = g.os[i] = q[i];
+    g.ks[i] = g.vs[i] = k[i];
+  }
+  g.q_rows = total_q;
+  g.k_rows = total_k;
+  g.map_b = 1;
+  g.grid_q = max_seqlen_q;
+  g.cu_q = cu_seqlens_q;
+  g.cu_k = cu_seqlens_k;
+  int dev;
+  attn_status st;
+  if ((st = get_device(&dev)) != ATTN_OK) return st;
+  uint32_t* status = nullptr;
+  if ((st = setup(dev, &status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Nq / Nk of the parameters are unused for packed sequences (each CTA reads its own)
+  if (d == 128)
+    return launch<128, false>(Q, K, V, O, LSE, B, H, max_seqlen_q, 0, scale, causal, nullptr, s, dev, status,
+                              StateOut{}, Variant{}, &g);
+  return launch<64, false>(Q, K, V, O, LSE, B, H, max_seqlen_q, 0, scale, causal, nullptr, s, dev, status,
+                           StateOut{}, Variant{}, &g);
 }
 
 attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,

@@ -33,6 +33,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -63,6 +64,13 @@ struct FwdParams {
   unsigned long long timeout_ns;
   int fault_block;         // test hook: the K block the producer never loads (-1: none)
   float tau;               // rescale threshold, log2 units: 0 = rescale whenever the max rises
+  // Layout.  Every tensor map is 4-D, (d, rows, heads, batches), over any strides.  Packed
+  // sequences (cu_q != null): sequence b is rows cu_q[b] .. cu_q[b+1] of Q / O and
+  // cu_k[b] .. cu_k[b+1] of K / V in maps with one batch; Nq and Nk are then per sequence.
+  const int32_t* cu_q;     // [B + 1] or null
+  const int32_t* cu_k;     // [B + 1] or null
+  int total_q, total_k;    // packed rows (the clamp for cu_q / cu_k)
+  __nv_bfloat16* o_packed; // packed sequences: O [total_q, H, D], for rows a TMA store would overrun
   // partial-state mode only: CTA (unit, split) absorbs key blocks [split * split_blocks,
   // (split + 1) * split_blocks) and writes the state (m, l, o~) instead of O and LSE
   int num_splits;          // >= 1
@@ -175,15 +183,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   int qtile = unit % nqt;
   if (p.causal) qtile = nqt - 1 - qtile;
   const int b = bh / p.H;
+  const int hh = bh - b * p.H;
   const int q0 = qtile * kBM;
-  int kv_len = p.Nk;
+  // this sequence: its first rows in the maps, its lengths, its batch coordinate
+  int q_base = 0, k_base = 0, Nq = p.Nq, Nk = p.Nk, bcoord = b;
+  if (p.cu_q) {
+    const int qs = min(max(__ldg(p.cu_q + b), 0), p.total_q);
+    const int qe = min(max(__ldg(p.cu_q + b + 1), qs), p.total_q);
+    const int ks = min(max(__ldg(p.cu_k + b), 0), p.total_k);
+    const int ke = min(max(__ldg(p.cu_k + b + 1), ks), p.total_k);
+    q_base = qs;
+    k_base = ks;
+    Nq = qe - qs;
+    Nk = ke - ks;
+    bcoord = 0;
+    if (q0 >= Nq) return;  // a tile past the end of a shorter sequence: nothing to do
+  }
+  int kv_len = Nk;
   if (p.lens) {
     const int L = __ldg(p.lens + b);
-    kv_len = L < 0 ? 0 : (L > p.Nk ? p.Nk : L);
+    kv_len = L < 0 ? 0 : (L > Nk ? Nk : L);
   }
-  const int qlast = min(q0 + kBM - 1, p.Nq - 1);
-  const int max_limit = row_key_limit(qlast, kv_len, p.Nq, p.Nk, p.causal);
-  const int min_limit = row_key_limit(q0, kv_len, p.Nq, p.Nk, p.causal);
+  const int qlast = min(q0 + kBM - 1, Nq - 1);
+  const int max_limit = row_key_limit(qlast, kv_len, Nq, Nk, p.causal);
+  const int min_limit = row_key_limit(q0, kv_len, Nq, Nk, p.causal);
   const int nvis = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;  // key blocks any row of the tile sees
   // this CTA absorbs key blocks jb0 .. jb0 + nblk - 1 (all of them unless it computes one split)
   const int jb0 = kStates ? split * p.split_blocks : 0;
@@ -227,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
       mbar_arrive_expect_tx(bar_q_full, C::kTileBytes);
-      for (int s = 0; s < C::kSub; ++s) tma_load_3d(sQ + s * C::kSubBytes, &tmQ, bar_q_full, s * 64, q0, bh, pol_q);
+      for (int s = 0; s < C::kSub; ++s)
+        tma_load_4d(sQ + s * C::kSubBytes, &tmQ, bar_q_full, s * 64, q_base + q0, hh, bcoord, pol_q);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nblk; ++j) {
         const int st = j % C::kStages;
@@ -236,15 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
           mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
           for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64, (jb0 + j) * kBN,
-                        bh, pol_kv);
+            tma_load_4d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64,
+                        k_base + (jb0 + j) * kBN, hh, bcoord, pol_kv);
         }
         k_issued = j + 1;
         if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) break;
         mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64, (jb0 + j) * kBN,
-                      bh, pol_kv);
+          tma_load_4d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64,
+                      k_base + (jb0 + j) * kBN, hh, bcoord, pol_kv);
         v_issued = j + 1;
       }
       // Let the last copies issued land before this warp leaves (in a normal run they were
@@ -315,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax / epilogue
     const int r = threadIdx.x;             // 0..127: row within the tile = tensor-memory lane
     const int row = q0 + r;
-    const int limit = row_key_limit(row, kv_len, p.Nq, p.Nk, p.causal);
+    const int limit = row_key_limit(row, kv_len, Nq, Nk, p.causal);
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float c = p.c;
     float m = -INFINITY;  // running max, log2 domain
@@ -460,6 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (!give_up) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint8_t* orow = smem + C::kOffQ + r * 128;
+      // The tile goes out by one TMA store, which clips rows past the end of the map.  The
+      // last tile of a packed sequence would overrun into the next sequence: its rows are
+      // stored one by one instead (the same for the whole CTA).
+      const bool direct = p.cu_q != nullptr && q0 + kBM > Nq;
+      uint4* grow = direct ? reinterpret_cast<uint4*>(p.o_packed + (static_cast<size_t>(q_base + min(row, Nq - 1)) *
+                                                                         p.H + hh) * D)
+                           : nullptr;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
@@ -479,19 +510,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv, __uint_as_float(o[ch * 8 + 5]) * inv);
           v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv, __uint_as_float(o[ch * 8 + 7]) * inv);
           const int chunk = (q % 2) * 4 + ch;
-          *reinterpret_cast<uint4*>(orow + (q / 2) * C::kSubBytes + ((chunk ^ (r & 7)) * 16)) = v;
+          if (direct) {
+            if (row < Nq) grow[q * 4 + ch] = v;
+          } else {
+            *reinterpret_cast<uint4*>(orow + (q / 2) * C::kSubBytes + ((chunk ^ (r & 7)) * 16)) = v;
+          }
         }
       }
-      if (row < p.Nq) {
+      if (row < Nq) {
         const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse;
+        // [B, H, Nq], or [H, total_q] for packed sequences
+        const size_t li = p.cu_q ? static_cast<size_t>(hh) * p.total_q + q_base + row
+                                 : static_cast<size_t>(bh) * p.Nq + row;
+        p.lse[li] = lse;
       }
-      fence_proxy_async_smem();
-      bar_sync_named(1, 128);
-      if (r == 0) {
-        for (int s = 0; s < C::kSub; ++s) tma_store_3d(&tmO, sQ + s * C::kSubBytes, s * 64, q0, bh);
-        tma_store_commit();
-        tma_store_wait_all();
+      if (!direct) {
+        fence_proxy_async_smem();
+        bar_sync_named(1, 128);
+        if (r == 0) {
+          for (int s = 0; s < C::kSub; ++s) tma_store_4d(&tmO, sQ + s * C::kSubBytes, s * 64, q_base + q0, hh, bcoord);
+          tma_store_commit();
+          tma_store_wait_all();
+        }
       }
     }
   }
