@@ -290,6 +290,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "splitkv"], default="fused")
+    ap.add_argument("--layout", choices=["bhsd", "bshd", "varlen"], default="bhsd")
     return ap.parse_args()
 
 
@@ -322,8 +323,9 @@ def l2_note(w):
     return f"no flush: working set {mb:.1f} MB fits in the 129 MB L2 (repeated steps hit L2)"
 
 
-def config_of(w, lens, world, path="fused", splits=1):
-    return {"workload": w["name"], "path": path if path == "fused" else f"splitkv (S={splits} + merge)", "B": w["B"], "H": w["H"], "Nq": w["Nq"], "Nk": w["Nk"], "d": w["d"],
+def config_of(w, lens, world, path="fused", splits=1, layout="bhsd"):
+    return {"workload": w["name"], "path": path if path == "fused" else f"splitkv (S={splits} + merge)",
+            "tensor_layout": {"bhsd": "[B,H,N,d] contiguous", "bshd": "[B,N,H,d] via attn_fwd_strided"}[layout], "B": w["B"], "H": w["H"], "Nq": w["Nq"], "Nk": w["Nk"], "d": w["d"],
             "causal": w["causal"], "key_padding": None if lens is None else [int(x) for x in lens],
             "layout": "[B,H,N,d] bf16, O bf16, LSE fp32",
             "l2": l2_note(w),
@@ -353,10 +355,84 @@ def reference_arm(args, w, lens, world, rank):
     print(json.dumps(out), flush=True)
 
 
+def timed_region(step, steps, stream, dev, pg, local, kernel_events=False):
+    """Time exactly `steps` calls of step() on `stream`, bracketed by a barrier and a
+    device synchronisation on both sides, with nvidia-smi clocks sampled meanwhile.
+    Returns (ms per step (max over ranks), ms of the dominant kernel per step, clocks).
+    With kernel_events, step(evs) records evs[0] / evs[1] around its dominant kernel."""
+    import torch
+    kev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+           if kernel_events else None)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark("t_start")
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            step(kev[i] if kev else None)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t_stop")
+    if pg:
+        pg.barrier()
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if pg:
+        t = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / steps
+    ms_kernel = ms_step if not kev else sum(a.elapsed_time(b) for a, b in kev) / steps
+    return ms_step, ms_kernel, clocks
+
+
+def e2e_region(e2e_step, steps, dev, pg):
+    """Wall time per call of e2e_step() (which copies in, computes, copies out and
+    synchronises), max over ranks."""
+    import torch
+    for _ in range(2):
+        e2e_step()
+    if pg:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / steps
+    if pg:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    return e2e_s
+
+
+def copy_e2e_step(stream, ins, step, outs):
+    """One end-to-end step through device buffers: pinned host -> device copies, the
+    step, device -> pinned host copies, then a synchronisation of the stream."""
+    import torch
+
+    def run():
+        with torch.cuda.stream(stream):
+            for host, devt in ins:
+                devt.copy_(host, non_blocking=True)
+            step()
+            for host, devt in outs:
+                host.copy_(devt, non_blocking=True)
+        stream.synchronize()
+    return run
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
     import gen
+    if args.layout == "varlen":
+        return main_varlen(args, world, rank, local)
     w = gen.WORKLOADS[args.workload]
     lens = gen.make_lens(w)
     if args.impl == "reference":
@@ -369,7 +445,7 @@ def main():
     from online_softmax_flashattention_attention_gb300 import build as pkgbuild
 
     pkgbuild.build_library()
-    pkg.load_library()
+    lib = pkg.load_library()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pg = None
@@ -395,32 +471,29 @@ def main():
     def dev_tensor(codes):
         return torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(dev)
 
+    def pinned(codes):
+        return torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).pin_memory()
+
     Q, K, V = dev_tensor(x["Q"]), dev_tensor(x["K"]), dev_tensor(x["V"])
     O = torch.empty_like(Q)
     LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
     lt = None if lens is None else torch.as_tensor(lens, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    flops = algorithmic_flops(B, H, Nq, Nk, d, causal, lens)
-
-    lib = pkg.load_library()
     sh = ctypes.c_void_p(stream.cuda_stream)
     lens_ptr = None if lt is None else lt.data_ptr()
-    fwd_args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d, scale,
-                int(causal), lens_ptr, sh)
+    flops = algorithmic_flops(B, H, Nq, Nk, d, causal, lens)
 
     def check(rc):
         if rc != 0:
             raise pkg.AttnError(rc, lib.attn_last_error().decode())
 
     splits = 1
-    if args.path == "fused":
-        launches_per_step = 1
-
-        def step(evs=None):
-            check(lib.attn_fwd(*fwd_args))
-    else:
+    kernel_events = False
+    e2e_api = None
+    if args.path == "splitkv":
         splits = pkg.splitkv_splits(B, H, Nq, Nk)
         launches_per_step = 2
+        kernel_events = True
         o_st = torch.empty((splits, B, H, Nq, d), dtype=torch.float32, device=dev)
         m_st = torch.empty((splits, B, H, Nq), dtype=torch.float32, device=dev)
         l_st = torch.empty((splits, B, H, Nq), dtype=torch.float32, device=dev)
@@ -436,123 +509,164 @@ def main():
             if evs:
                 evs[1].record(stream)
             check(lib.attn_merge_states(*mg_args))
+        e2e_api = "attn_fwd_states + attn_merge_states (C ABI) with pinned host copies inside the timed region"
+    elif args.layout == "bshd":
+        # the same values stored [B, N, H, d]; the tensors handed over are [B, H, N, d] views
+        launches_per_step = 1
+        Q, K, V = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (Q, K, V))
+        O = torch.empty((B, Nq, H, d), dtype=torch.bfloat16, device=dev).transpose(1, 2)
+        strides = [(ctypes.c_int64 * 3)(*t.stride()[:3]) for t in (Q, K, V, O)]
+        sd_args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d, scale,
+                   int(causal), lens_ptr, *strides, sh)
+
+        def step(evs=None):
+            check(lib.attn_fwd_strided(*sd_args))
+        e2e_api = "attn_fwd_strided (C ABI, [B, N, H, d] tensors) with pinned host copies inside the timed region"
+    else:
+        launches_per_step = 1
+        fwd_args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d, scale,
+                    int(causal), lens_ptr, sh)
+
+        def step(evs=None):
+            check(lib.attn_fwd(*fwd_args))
 
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
             step()
     pkg.status_sync(stream)
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    sampler.mark("t_start")
-    # split path: events around every states launch give that kernel's own duration
-    kev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)] if args.path == "splitkv" else None)
-    ev0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(args.steps):
-            step(kev[i] if kev else None)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    sampler.mark("t_stop")
-    if pg:
-        pg.barrier()
-    clocks = sampler.stop()
+    ms_step, ms_kernel, clocks = timed_region(step, args.steps, stream, dev, pg, local, kernel_events)
     pkg.status_sync(stream)
-    ms_total = ev0.elapsed_time(ev1)
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
-    ms_step = ms_total / args.steps
     value = world * flops / (ms_step * 1e-3) / 1e12
-    ms_kernel = ms_step if not kev else sum(a.elapsed_time(b) for a, b in kev) / args.steps
     per_launch_tflops = flops / (ms_kernel * 1e-3) / 1e12
-
-    # ---- end to end through the host-buffer C entry point (pinned host memory)
+    # ---- end to end: pinned host buffers, copies in and out inside the timed region
     e2e = None
-    if args.e2e_steps > 0 and args.path == "splitkv":
-        # the same two C calls, fed from pinned host buffers copied in and out every step
-        Qh, Kh, Vh = (torch.from_numpy(c.view(np.int16)).view(torch.bfloat16).pin_memory()
-                      for c in (x["Q"], x["K"], x["V"]))
-        Oh = torch.empty_like(Qh).pin_memory()
-        Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    if args.e2e_steps > 0:
+        if e2e_api is None:  # the host-buffer C entry point does the copies itself
+            Qh, Kh, Vh = pinned(x["Q"]), pinned(x["K"]), pinned(x["V"])
+            Oh = torch.empty_like(Qh).pin_memory()
+            Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+            lh = None if lens is None else torch.as_tensor(lens, dtype=torch.int32)
 
-        def e2e_step():
-            with torch.cuda.stream(stream):
-                Q.copy_(Qh, non_blocking=True)
-                K.copy_(Kh, non_blocking=True)
-                V.copy_(Vh, non_blocking=True)
-                step()
-                Oh.copy_(O, non_blocking=True)
-                Lh.copy_(LSE, non_blocking=True)
-            stream.synchronize()
-
-        for _ in range(2):
-            e2e_step()
-        if pg:
-            pg.barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-        if pg:
-            t = torch.tensor([e2e_s], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": (Qh.numel() + Kh.numel() + Vh.numel()) * 2,
-               "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4, "ms_per_step": e2e_s * 1e3,
-               "api": "attn_fwd_states + attn_merge_states (C ABI) with pinned host copies inside the timed region"}
-    elif args.e2e_steps > 0:
-        def pinned(codes):
-            return torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).pin_memory()
-
-        Qh, Kh, Vh = pinned(x["Q"]), pinned(x["K"]), pinned(x["V"])
-        Oh = torch.empty_like(Qh).pin_memory()
-        Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
-        lh = None if lens is None else torch.as_tensor(lens, dtype=torch.int32)
-        for _ in range(2):
-            pkg.attn_fwd_host(Qh, Kh, Vh, Oh, Lh, scale=scale, causal=causal, key_padding_lens=lh, stream=stream)
-        if pg:
-            pg.barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            pkg.attn_fwd_host(Qh, Kh, Vh, Oh, Lh, scale=scale, causal=causal, key_padding_lens=lh, stream=stream)
-        e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-        if pg:
-            t = torch.tensor([e2e_s], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        h2d = Qh.numel() * 2 + Kh.numel() * 2 + Vh.numel() * 2 + (0 if lh is None else lh.numel() * 4)
-        d2h = Oh.numel() * 2 + Lh.numel() * 4
+            def e2e_step():
+                pkg.attn_fwd_host(Qh, Kh, Vh, Oh, Lh, scale=scale, causal=causal, key_padding_lens=lh, stream=stream)
+            e2e_api = "attn_fwd_host (C ABI, pinned host buffers, copies inside the timed region)"
+            h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * 2 + (0 if lh is None else lh.numel() * 4)
+        else:
+            # host buffers with the device tensors' strides: every copy is one plain memcpy
+            hosts = [torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, pin_memory=True) for t in (Q, K, V)]
+            for hst, t in zip(hosts, (Q, K, V)):
+                hst.copy_(t.cpu())
+            Oh = torch.empty_strided(O.shape, O.stride(), dtype=O.dtype, pin_memory=True)
+            Lh = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+            e2e_step = copy_e2e_step(stream, list(zip(hosts, (Q, K, V))), step, [(Oh, O), (Lh, LSE)])
+            h2d = sum(h.numel() for h in hosts) * 2
+        e2e_s = e2e_region(e2e_step, args.e2e_steps, dev, pg)
         e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-               "api": "attn_fwd_host (C ABI, pinned host buffers, copies inside the timed region)"}
+               "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4, "ms_per_step": e2e_s * 1e3, "api": e2e_api}
 
     peak, peak_src = load_peaks()
     hbm_peak, hbm_src = load_hbm_peak()
     kbytes = algorithmic_bytes(B, H, Nq, Nk, d, lens, 0 if args.path == "fused" else splits)
     intensity = flops / kbytes
     ridge = peak * 1e12 / (hbm_peak * 1e9)
-    traffic = load_traffic(w["name"] if args.path == "fused" else w["name"] + ":splitkv")
+    key = w["name"] + ("" if args.path == "fused" else ":splitkv") + ("" if args.layout == "bhsd" else ":" + args.layout)
+    traffic = load_traffic(key)
+    kname = f"attn_fwd_kernel<{d}>" + ("" if args.path == "fused" else " (states)")
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": config_of(w, lens, world, args.path, splits),
+           "config": config_of(w, lens, world, args.path, splits, args.layout),
            "roofline": roofline_entry(intensity, ridge, per_launch_tflops, peak, peak_src, kbytes, ms_kernel,
-                                      hbm_peak, hbm_src, traffic, flops,
-                                      f"attn_fwd_kernel<{d}>" + ("" if args.path == "fused" else " (states)")),
+                                      hbm_peak, hbm_src, traffic, flops, kname),
            "e2e": e2e,
            "gpu_launches": args.steps * launches_per_step,
            "clocks": clocks,
            "cpu_baseline": cpu}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def main_varlen(args, world, rank, local):
+    """--layout varlen: a packed workload of sequences of different lengths through
+    attn_fwd_varlen.  Flops count every sequence's causal triangle as n^2 / 2."""
+    import gen
+    import numpy as np
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    from online_softmax_flashattention_attention_gb300 import build as pkgbuild
+
+    name = args.workload if args.workload in gen.VARLEN_WORKLOADS else "varlen_causal_b16h16d128"
+    x = gen.make_varlen(name)
+    B, H, d, total = x["B"], x["H"], x["d"], x["total"]
+    lengths = [int(n) for n in x["lengths"]]
+    causal, scale = x["causal"], x["scale"]
+    pairs = sum(n * n / 2.0 if causal else float(n * n) for n in lengths)
+    flops = 4.0 * H * d * pairs
+    config = {"workload": name, "layout": "packed [total, H, d] bf16, LSE [H, total] fp32", "B": B, "H": H, "d": d,
+              "causal": causal, "lengths": lengths, "total_rows": total,
+              "l2": f"no flush: inputs and outputs larger than L2 ({(4 * total * H * d * 2 + 4 * H * total) / 1e6:.0f}"
+                    " MB per step vs 129 MB L2)",
+              "parallelism": f"replicas x{world} (each rank its own problem)"}
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm runs on the dense workloads; "
+                              "packed sequences are timed against the dense route of the same library only"}))
+        return
+    pkgbuild.build_library()
+    lib = pkg.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    to_dev = lambda c: torch.from_numpy(c.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+    Q, K, V = to_dev(x["Q"]), to_dev(x["K"]), to_dev(x["V"])
+    O = torch.empty_like(Q)
+    LSE = torch.empty((H, total), dtype=torch.float32, device=dev)
+    cu = torch.as_tensor(x["cu"], dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    args_v = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), cu.data_ptr(), cu.data_ptr(),
+              B, H, max(lengths), total, total, d, scale, int(causal), sh)
+
+    def step(evs=None):
+        rc = lib.attn_fwd_varlen(*args_v)
+        if rc != 0:
+            raise pkg.AttnError(rc, lib.attn_last_error().decode())
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    pkg.status_sync(stream)
+    ms_step, ms_kernel, clocks = timed_region(step, args.steps, stream, dev, pg, local)
+    pkg.status_sync(stream)
+    tflops = flops / (ms_step * 1e-3) / 1e12
+    e2e = None
+    if args.e2e_steps > 0:
+        hosts = [torch.from_numpy(c.view(np.int16)).view(torch.bfloat16).pin_memory() for c in (x["Q"], x["K"], x["V"])]
+        Oh = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+        Lh = torch.empty(LSE.shape, dtype=LSE.dtype).pin_memory()
+        e2e_s = e2e_region(copy_e2e_step(stream, list(zip(hosts, (Q, K, V))), step, [(Oh, O), (Lh, LSE)]),
+                           args.e2e_steps, dev, pg)
+        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(h.numel() for h in hosts) * 2,
+               "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4, "ms_per_step": e2e_s * 1e3,
+               "api": "attn_fwd_varlen (C ABI) with pinned host copies inside the timed region"}
+    peak, peak_src = load_peaks()
+    hbm_peak, hbm_src = load_hbm_peak()
+    kbytes = 2.0 * H * d * 4 * total + 4.0 * H * total
+    out = {"metric": METRIC, "value": world * tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+           "roofline": roofline_entry(flops / kbytes, peak * 1e12 / (hbm_peak * 1e9), tflops, peak, peak_src, kbytes,
+                                      ms_kernel, hbm_peak, hbm_src, load_traffic(name), flops,
+                                      f"attn_fwd_kernel<{d}> (packed sequences)"),
+           "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": None}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg:

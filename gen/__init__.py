@@ -247,3 +247,30 @@ def make_inputs(w, **override) -> dict:
         out["Q"], out["planted_key"] = plant_scores(Q, K, lens, w["scale"], p["score"], p["tile"], seed)
     return out
 
+
+
+# --- packed sequences of different lengths --------------------------------------
+
+VARLEN_WORKLOADS = {
+    # 16 prompts of 512..8192 tokens (seeded uniform), 16 heads, d = 128, causal within
+    # each prompt, N(0, 1) values, packed row after row: [total, H, d]
+    "varlen_causal_b16h16d128": dict(name="varlen_causal_b16h16d128", B=16, H=16, d=128, causal=True,
+                                     lengths=("uniform", 512, 8192), qk=("normal", 0.0, 1.0),
+                                     v=("normal", 0.0, 1.0), seed=1008),
+}
+
+
+def make_varlen(name: str) -> dict:
+    """Packed inputs: Q, K, V codes [total, H, d], cu [B + 1] (the same for queries and
+    keys), lengths, scale, causal."""
+    w = VARLEN_WORKLOADS[name]
+    lo, hi = w["lengths"][1], w["lengths"][2]
+    lengths = uniform_int(w["B"], w["seed"], TID_LENS, lo, hi).astype(np.int64)
+    total = int(lengths.sum())
+    shape = (total, w["H"], w["d"])
+    Q = _draw(w["qk"], shape, w["seed"], TID_Q)
+    K = _draw(w["qk"], shape, w["seed"], TID_K)
+    V = _draw(w["v"], shape, w["seed"], TID_V)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    return dict(name=name, Q=Q, K=K, V=V, cu=cu, lengths=lengths, total=total, B=w["B"], H=w["H"], d=w["d"],
+                causal=w["causal"], scale=1.0 / math.sqrt(w["d"]))
