@@ -468,6 +468,22 @@ def main():
     B, H, Nq, Nk, d = x["B"], x["H"], x["Nq"], x["Nk"], x["d"]
     scale, causal = x["scale"], x["causal"]
 
+    # the blocked CPU library on a sample of whole heads (host only, before any GPU work)
+    cpu_blocked = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from online_softmax_flashattention_attention_gb300 import build as pkgb
+        pkgb.build_cpu_library()
+        per_head = algorithmic_flops(B, 1, Nq, Nk, d, causal, lens)
+        hs = max(1, min(H, int(round(40e9 / max(per_head, 1.0)))))
+        sub = [np.ascontiguousarray(x[t][:, :hs]) for t in ("Q", "K", "V")]
+        pkg.attn_fwd_cpu(*[a[:, :1, :min(Nq, 256)] for a in sub], scale=scale)   # load + warm the library
+        t0 = time.perf_counter()
+        pkg.attn_fwd_cpu(*sub, scale=scale, causal=causal, key_padding_lens=lens)
+        secs = time.perf_counter() - t0
+        cpu_blocked = {"value": per_head * hs / secs / 1e12, "unit": "TFLOP/s", "cores": host_cores(),
+                       "kind": "blocked C library (libattn_cpu.so, fp32, one thread per core)",
+                       "sample": f"all rows of heads 0..{hs - 1} of every batch of {w['name']} ({secs:.2f} s)"}
+
     def dev_tensor(codes):
         return torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(dev)
 
@@ -581,7 +597,8 @@ def main():
            "e2e": e2e,
            "gpu_launches": args.steps * launches_per_step,
            "clocks": clocks,
-           "cpu_baseline": cpu}
+           "cpu_baseline": cpu,
+           "cpu_blocked": cpu_blocked}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg:

@@ -340,3 +340,46 @@ def attn_fwd_varlen(Q, K, V, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, O=None, L
                                         total_q, total_k, d, float(scale), int(causal), _stream_handle(stream))
     _check(rc)
     return O, LSE
+
+
+# --- the CPU library (libattn_cpu.so, include/attn_cpu.h) ------------------------
+
+CPU_LIB_PATH = os.path.join(_HERE, "libattn_cpu.so")
+CPU_EXPORTS = ("attn_fwd_cpu",)
+_cpu_lib = None
+
+
+def load_cpu_library():
+    """Load libattn_cpu.so (built by __graft_entry__.build()); raises if it is absent."""
+    global _cpu_lib
+    if _cpu_lib is None:
+        if not os.path.exists(CPU_LIB_PATH):
+            raise ImportError(f"{CPU_LIB_PATH} is missing: build it with __graft_entry__.build()")
+        lib = ctypes.CDLL(CPU_LIB_PATH)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        lib.attn_fwd_cpu.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp, i]
+        lib.attn_fwd_cpu.restype = i
+        _cpu_lib = lib
+    return _cpu_lib
+
+
+def attn_fwd_cpu(Q, K, V, *, scale=None, causal=False, key_padding_lens=None, num_threads=0):
+    """The forward on the host CPU.  Q [B,H,Nq,d], K/V [B,H,Nk,d]: numpy uint16 arrays of
+    bf16 codes.  Returns O (uint16 codes, same shape as Q) and LSE (float32 [B,H,Nq])."""
+    import numpy as np
+    Q, K, V = (np.ascontiguousarray(a, dtype=np.uint16) for a in (Q, K, V))
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
+    if K.shape != (B, H, Nk, d) or V.shape != (B, H, Nk, d):
+        raise ValueError("K and V must be [B, H, Nk, d] with Q's B, H and d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    O = np.empty_like(Q)
+    LSE = np.empty((B, H, Nq), dtype=np.float32)
+    lens = None if key_padding_lens is None else np.ascontiguousarray(key_padding_lens, dtype=np.int32)
+    rc = load_cpu_library().attn_fwd_cpu(Q.ctypes.data, K.ctypes.data if Nk else None, V.ctypes.data if Nk else None,
+                                         O.ctypes.data, LSE.ctypes.data, B, H, Nq, Nk, d, float(scale), int(causal),
+                                         None if lens is None else lens.ctypes.data, int(num_threads))
+    if rc != 0:
+        raise AttnError(rc, "attn_fwd_cpu failed")
+    return O, LSE
