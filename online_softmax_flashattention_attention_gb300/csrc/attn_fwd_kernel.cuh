@@ -345,10 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY;  // running max, log2 domain
     float l = 0.f;        // running denominator
     bool ok = true;
+    // Checking a barrier costs a long round trip even when its phase completed long ago.
+    // The two checks of every block are therefore issued early, as non-blocking tests
+    // whose results are consumed later: s_full of the next block during this block's
+    // exponentials, pv_done of the previous block halfway through them.  Only when a test
+    // says "not yet" does the thread take the (bounded) wait.
+    bool s_seen = false;  // s_full of block j already seen complete
     for (int j = 0; j < nblk; ++j) {
       const uint32_t colS = C::col_s(j % kSBufs);
       // every lane of the warp takes the same branch: the tcgen05 loads below are warp-wide
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(j % kSBufs), (j / kSBufs) & 1, wc, 9));
+      if (!__all_sync(0xffffffffu, s_seen))
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(j % kSBufs), (j / kSBufs) & 1, wc, 9));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[kBN];
@@ -384,10 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 c2 = make_float2(c, c);
       const float2 nm2 = make_float2(-m_ref, -m_ref);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      bool pv_seen = false;  // pv_done of block j - 1 seen complete
       auto exp_block = [&](auto soft_tag) {
         constexpr bool kSoft = decltype(soft_tag)::value;
 #pragma unroll
         for (int q = 0; q < kBN / 32; ++q) {
+          if (q == 0)
+            s_seen = j + 1 < nblk && mbar_test_wait(bar_s_full((j + 1) % kSBufs), ((j + 1) / kSBufs) & 1);
+          if (q == 2)
+            pv_seen = j > 0 && mbar_test_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1);
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -417,8 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_new;
       if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
         // o~ may be touched only after the previous P V product has landed in it
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, wc, 10));
+        if (!__all_sync(0xffffffffu, pv_seen))
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, wc, 10));
         if (!ok) break;
         tc_fence_after();
         const float2 al2 = make_float2(alpha, alpha);
