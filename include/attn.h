@@ -26,8 +26,8 @@
  *  - A row with no visible key (fully masked, or Nk == 0) gets O = 0 and LSE = -inf,
  *    never 0/0.
  *  - d must be 64 or 128.  scale must be finite and > 0 (1/sqrt(d) is the usual value).
- *  - All device pointers must be 16-byte aligned (TMA); the library does not check that
- *    they are device pointers.
+ *  - Q, K, V and O must be 16-byte aligned (TMA), LSE 4-byte aligned; the library does
+ *    not check that they are device pointers.
  *
  * Ownership: the caller owns every buffer.  attn_fwd allocates no device memory per
  * call; the library keeps one small device status word per device, created on first use.
@@ -143,10 +143,14 @@ attn_status attn_fwd_varlen(const void* Q, const void* K, const void* V, void* O
 
 /*
  * attn_fwd_host -- the same operation on HOST buffers (pinned memory recommended).
- * Copies Q, K, V (and key_padding_lens, a host int32[B] or NULL) to the device on
- * `stream`, runs attn_fwd, copies O and LSE back and synchronises the stream before it
- * returns.  Uses a per-device workspace that grows to the largest problem seen and is
- * kept until attn_release_workspace(); it allocates only when a call needs more room.
+ * Copies Q, K, V (and key_padding_lens, a host int32[B] or NULL) to the device, runs the
+ * forward, copies O and LSE back and synchronises `stream` before it returns.  The copies
+ * run on two streams of the library's own, overlapped with the forward on `stream`: the
+ * heads are cut into chunks (runs of heads of one batch, about 32 MB of input each) and
+ * chunk i is computed while chunk i + 1 is copied in and chunk i - 1 copied out.  The
+ * work starts after what is already queued on `stream`.  Uses a per-device workspace
+ * that grows to the largest problem seen and is kept until attn_release_workspace(); it
+ * allocates only when a call needs more room (and creates its two streams once).
  */
 attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                           int Nq, int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,

@@ -76,6 +76,45 @@ attn_status setup(int dev, uint32_t** status) {
   return ATTN_OK;
 }
 
+// attn_fwd_host's copy streams and events, one set per device, created on first use.
+constexpr int kHostEvents = 64;  // event slots, reused round robin (more than any chunk count)
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+  cudaEvent_t ev_in[kHostEvents] = {}, ev_done[kHostEvents] = {};
+};
+HostPipe* g_pipe[kMaxDevices] = {};
+
+attn_status host_pipe(int dev, HostPipe** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_pipe[dev]) {
+    HostPipe* hp = new HostPipe;
+    cudaError_t e = cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_end, cudaEventDisableTiming);
+    for (int i = 0; i < kHostEvents && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&hp->ev_in[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->ev_done[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "copy streams / events: %s", cudaGetErrorString(e));
+    g_pipe[dev] = hp;
+  }
+  *out = g_pipe[dev];
+  return ATTN_OK;
+}
+
+// How many chunks attn_fwd_host cuts a problem into: about one per 32 MB of input, at
+// least one per batch, at most 16 (plus one per extra batch) -- enough to overlap the
+// copies with the forward, few enough that every chunk's grid still fills the GPU.
+int host_chunks(int B, int H, size_t in_bytes) {
+  const long long want = static_cast<long long>(in_bytes / (32u << 20));
+  long long n = std::max<long long>(1, std::min<long long>(16, want));
+  n = std::min<long long>(n, static_cast<long long>(B) * H);
+  return static_cast<int>(std::max<long long>(n, B));
+}
+int nch_per_batch(int nch, int B) { return std::max(1, nch / std::max(1, B)); }
+
 // Where the four tensors live.  Each is seen through a 4-D map (d, rows, heads,
 // batches) with element strides (batch, head, row); d is contiguous.  Packed sequences
 // use one batch and the per-sequence row offsets cu_q / cu_k.
@@ -153,8 +192,9 @@ attn_status check_args(const void* Q, const void* K, const void* V, void* O, flo
   if (BH == 0 || Nq == 0) return ATTN_OK;
   if (!Q || !O || !LSE) return fail(ATTN_ERR_NULLPTR, "Q, O and LSE must not be NULL");
   if (Nk > 0 && (!K || !V)) return fail(ATTN_ERR_NULLPTR, "K and V must not be NULL when Nk > 0");
-  if (misaligned(Q) || misaligned(O) || misaligned(LSE) || (Nk > 0 && (misaligned(K) || misaligned(V))))
-    return fail(ATTN_ERR_MISALIGNED, "pointers must be 16-byte aligned");
+  if (misaligned(Q) || misaligned(O) || (Nk > 0 && (misaligned(K) || misaligned(V))))
+    return fail(ATTN_ERR_MISALIGNED, "Q, K, V and O must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(LSE) & 3u) return fail(ATTN_ERR_MISALIGNED, "LSE must be 4-byte aligned");
   return ATTN_OK;
 }
 
@@ -427,19 +467,55 @@ attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, 
   uint8_t* dV = dK + up(kv_bytes);
   float* dL = reinterpret_cast<float*>(dV + up(kv_bytes));
   int32_t* dlens = key_padding_lens ? reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(dL) + up(lse_bytes)) : nullptr;
+  HostPipe* hp = nullptr;
+  if ((st = host_pipe(dev, &hp)) != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(dQ, Q, q_bytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && kv_bytes) e = cudaMemcpyAsync(dK, K, kv_bytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && kv_bytes) e = cudaMemcpyAsync(dV, V, kv_bytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && lens_bytes) e = cudaMemcpyAsync(dlens, key_padding_lens, lens_bytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "host-to-device copy: %s", cudaGetErrorString(e));
-  st = attn_fwd(dQ, kv_bytes ? dK : nullptr, kv_bytes ? dV : nullptr, dO, dL, B, H, Nq, Nk, d, scale, causal, dlens,
-                stream);
-  if (st != ATTN_OK) return st;
-  e = cudaMemcpyAsync(O, dO, q_bytes, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(LSE, dL, lse_bytes, cudaMemcpyDeviceToHost, s);
+  // The copies run on two streams of their own, overlapped with the forward on `stream`:
+  // chunk i (a run of heads of one batch) is copied in, computed, and copied out while
+  // chunk i + 1 is copied in.  Chunks start after the work already queued on `stream`,
+  // and `stream` waits for the last copy out, so the call keeps stream order.
+  const int nch = host_chunks(B, H, q_bytes + 2 * kv_bytes);
+  cudaError_t e = cudaEventRecord(hp->ev_start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->ev_start, 0);
+  if (e == cudaSuccess && lens_bytes)
+    e = cudaMemcpyAsync(dlens, key_padding_lens, lens_bytes, cudaMemcpyHostToDevice, hp->in);
+  const size_t qh = static_cast<size_t>(Nq) * d * 2, kh = static_cast<size_t>(Nk) * d * 2;  // bytes per head
+  int done = 0;
+  for (int b = 0; b < B && e == cudaSuccess; ++b) {
+    for (int h0 = 0; h0 < H && e == cudaSuccess; ++done) {
+      const int hc = std::min(H - h0, (H + nch_per_batch(nch, B) - 1) / nch_per_batch(nch, B));
+      const size_t bh0 = static_cast<size_t>(b) * H + h0;
+      const int slot = done % kHostEvents;
+      // the slot's events were last used kHostEvents chunks ago: their work is queued ahead
+      e = cudaMemcpyAsync(dQ + bh0 * qh, static_cast<const uint8_t*>(Q) + bh0 * qh, hc * qh, cudaMemcpyHostToDevice,
+                          hp->in);
+      if (e == cudaSuccess && kh)
+        e = cudaMemcpyAsync(dK + bh0 * kh, static_cast<const uint8_t*>(K) + bh0 * kh, hc * kh,
+                            cudaMemcpyHostToDevice, hp->in);
+      if (e == cudaSuccess && kh)
+        e = cudaMemcpyAsync(dV + bh0 * kh, static_cast<const uint8_t*>(V) + bh0 * kh, hc * kh,
+                            cudaMemcpyHostToDevice, hp->in);
+      if (e == cudaSuccess) e = cudaEventRecord(hp->ev_in[slot], hp->in);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->ev_in[slot], 0);
+      if (e != cudaSuccess) break;
+      st = attn_fwd(dQ + bh0 * qh, kh ? dK + bh0 * kh : nullptr, kh ? dV + bh0 * kh : nullptr, dO + bh0 * qh,
+                    dL + bh0 * Nq, 1, hc, Nq, Nk, d, scale, causal, dlens ? dlens + b : nullptr, stream);
+      if (st != ATTN_OK) return st;
+      e = cudaEventRecord(hp->ev_done[slot], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->ev_done[slot], 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(static_cast<uint8_t*>(O) + bh0 * qh, dO + bh0 * qh, hc * qh, cudaMemcpyDeviceToHost,
+                            hp->out);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(LSE + bh0 * Nq, dL + bh0 * Nq, static_cast<size_t>(hc) * Nq * 4, cudaMemcpyDeviceToHost,
+                            hp->out);
+      h0 += hc;
+    }
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(hp->ev_end, hp->out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->ev_end, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "device-to-host copy: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "host-buffer pipeline: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }
 

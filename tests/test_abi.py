@@ -47,7 +47,7 @@ def test_library_is_sm103a_only():
     (dict(d=96), -3), (dict(d=0), -3), (dict(B=-1), -2), (dict(Nk=-5), -2), (dict(scale=0.0), -8),
     (dict(scale=-0.1), -8), (dict(scale=float("nan")), -8), (dict(scale=float("inf")), -8),
     (dict(Q=0), -1), (dict(O=0), -1), (dict(LSE=0), -1), (dict(K=0), -1), (dict(V=0), -1),
-    (dict(Q=0x1008), -4), (dict(LSE=0x2004), -4), (dict(V=0x3002), -4),
+    (dict(Q=0x1008), -4), (dict(LSE=0x2002), -4), (dict(V=0x3002), -4),
 ])
 def test_argument_errors(lib, args, status):
     a = dict(Q=0x10000, K=0x20000, V=0x30000, O=0x40000, LSE=0x50000, B=1, H=2, Nq=256, Nk=256, d=64,

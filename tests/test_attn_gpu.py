@@ -226,6 +226,29 @@ def test_host_buffer_entry_point():
     assert np.array_equal(Oh.float().numpy(), O_dev) and np.array_equal(Lh.numpy(), LSE_dev)
 
 
+@pytest.mark.parametrize("B,H,N,causal,lens", [(1, 12, 8192, True, None), (2, 10, 4096, False, [4096, 1500])])
+def test_host_entry_point_pipelined_chunks(B, H, N, causal, lens):
+    """Inputs big enough for attn_fwd_host to cut the heads into several chunks (uneven
+    ones in the first case) whose copies overlap the forward: the result must equal the
+    device entry point bit for bit, and the oracle on sampled rows."""
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    x = custom(B, H, N, N, 128, causal, seed=77 + B, lens=lens)
+    pin = lambda c: torch.from_numpy(np.ascontiguousarray(c).view(np.int16)).view(torch.bfloat16).pin_memory()  # noqa
+    Qh, Kh, Vh = pin(x["Q"]), pin(x["K"]), pin(x["V"])
+    Oh = torch.full_like(Qh, float("nan")).pin_memory()
+    Lh = torch.full((B, H, N), float("nan"), dtype=torch.float32).pin_memory()
+    lh = None if lens is None else torch.as_tensor(np.asarray(lens, np.int32))
+    pkg.attn_fwd_host(Qh, Kh, Vh, Oh, Lh, scale=x["scale"], causal=causal, key_padding_lens=lh)
+    O_dev, L_dev = run_cuda(x)
+    assert np.array_equal(Oh.float().numpy().astype(np.float64), O_dev)
+    assert np.array_equal(Lh.numpy().astype(np.float64), L_dev)
+    picks = sample_rows(B, H, N, n_random=16, seed=3)
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"], picks)
+    idx = tuple(np.array(picks).T)
+    compare(O_dev[idx], L_dev[idx], O_ref, LSE_ref)
+
+
 def test_canary_guard_bands_untouched():
     import torch
     import online_softmax_flashattention_attention_gb300 as pkg
