@@ -474,7 +474,7 @@ def main():
         from online_softmax_flashattention_attention_gb300 import build as pkgb
         pkgb.build_cpu_library()
         per_head = algorithmic_flops(B, 1, Nq, Nk, d, causal, lens)
-        hs = max(1, min(H, int(round(40e9 / max(per_head, 1.0)))))
+        hs = max(1, min(H, int(round(400e9 / max(per_head, 1.0)))))
         sub = [np.ascontiguousarray(x[t][:, :hs]) for t in ("Q", "K", "V")]
         pkg.attn_fwd_cpu(*[a[:, :1, :min(Nq, 256)] for a in sub], scale=scale)   # load + warm the library
         t0 = time.perf_counter()
