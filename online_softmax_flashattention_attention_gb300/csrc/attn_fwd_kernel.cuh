@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = j % C::kStages;
           // V_j has normally landed long before P_j is ready: check it first
           ok = mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 7) &&
-               mbar_wait(bar_p_full(j % kSBufs), (j / kSBufs) & 1, wc, 6);
+               mbar_wait_poll(bar_p_full(j % kSBufs), (j / kSBufs) & 1, wc, 6);
           if (!ok) break;
           tc_fence_after();
           // o~ += P_j V_j: 8 k-steps of 16 keys; A = P_j from tensor memory, B = V_j MN-major
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Checking a barrier costs a long round trip even when its phase completed long ago.
     // The two checks of every block are therefore issued early, as non-blocking tests
     // whose results are consumed later: s_full of the next block during this block's
-    // exponentials, pv_done of the previous block halfway through them.  Only when a test
+    // exponentials, pv_done of the previous block before their last chunk.  Only when a test
     // says "not yet" does the thread take the (bounded) wait.
     bool s_seen = false;  // s_full of block j already seen complete
     for (int j = 0; j < nblk; ++j) {
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < kBN / 32; ++q) {
           if (q == 0)
             s_seen = j + 1 < nblk && mbar_test_wait(bar_s_full((j + 1) % kSBufs), ((j + 1) / kSBufs) & 1);
-          if (q == 2)
+          if (q == 3)
             pv_seen = j > 0 && mbar_test_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1);
           uint32_t pk[16];
 #pragma unroll

@@ -90,6 +90,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// The same bounded wait by polling with non-blocking tests, for a thread that has nothing
+// else to do and must react as soon as the phase completes: a suspended try_wait can take
+// a few hundred cycles to resume after the completion.  The abort word and the time limit
+// are checked every 32 polls.
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort_flag = 1u;
+        if (w.status) atomicOr(w.status, 1u | (site << 8));
+        return false;
+      }
+    }
+  }
+}
+
 // Wait that ignores the abort word and records nothing: used only to let work already
 // in flight (TMA copies, MMAs) finish before a CTA that gave up releases its resources.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
