@@ -356,6 +356,23 @@ def reference_arm(args, w, lens, world, rank):
     print(json.dumps(out), flush=True)
 
 
+def max_over_ranks(x: float, pg, device) -> float:
+    """The largest value of x over the ranks of the process group (x itself without one):
+    the job's time is its slowest rank's."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_rank: float, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank ran its own copy of the workload (weak scaling), and the
+    job took as long as its slowest rank."""
+    return world * flops_per_rank / seconds / 1e12
+
+
 def timed_region(step, steps, stream, dev, pg, local, kernel_events=False):
     """Time exactly `steps` calls of step() on `stream`, bracketed by a barrier and a
     device synchronisation on both sides, with nvidia-smi clocks sampled meanwhile.
@@ -383,11 +400,7 @@ def timed_region(step, steps, stream, dev, pg, local, kernel_events=False):
     if pg:
         pg.barrier()
     clocks = sampler.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     ms_step = ms_total / steps
     ms_kernel = ms_step if not kev else sum(a.elapsed_time(b) for a, b in kev) / steps
     return ms_step, ms_kernel, clocks
@@ -404,12 +417,7 @@ def e2e_region(e2e_step, steps, dev, pg):
     t0 = time.perf_counter()
     for _ in range(steps):
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / steps
-    if pg:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    return e2e_s
+    return max_over_ranks((time.perf_counter() - t0) / steps, pg, dev)
 
 
 def copy_e2e_step(stream, ins, step, outs):
@@ -553,7 +561,7 @@ def main():
     pkg.status_sync(stream)
     ms_step, ms_kernel, clocks = timed_region(step, args.steps, stream, dev, pg, local, kernel_events)
     pkg.status_sync(stream)
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms_step * 1e-3)
     per_launch_tflops = flops / (ms_kernel * 1e-3) / 1e12
 
     # the lazy-rescale option on the same inputs (not the headline: the pages' rule is)
