@@ -76,6 +76,17 @@ attn_status setup(int dev, uint32_t** status) {
   return ATTN_OK;
 }
 
+// SM count of a device, cached.
+int sm_count(int dev) {
+  static int cached[kMaxDevices] = {};
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // attn_fwd_host's copy streams and events, one set per device, created on first use.
 constexpr int kHostEvents = 64;  // event slots, reused round robin (more than any chunk count)
 struct HostPipe {
@@ -280,9 +291,16 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   p.cu_k = geo.cu_k;
   p.total_q = static_cast<int>(geo.q_rows);
   p.total_k = static_cast<int>(geo.k_rows);
-  p.o_packed = static_cast<__nv_bfloat16*>(O);
-  const unsigned grid = static_cast<unsigned>(p.num_qtiles) * static_cast<unsigned>(BH) *
-                        static_cast<unsigned>(p.num_splits);
+  p.o = static_cast<__nv_bfloat16*>(O);
+  p.os_b = geo.cu_q ? 0 : geo.os[0];  // packed sequences address rows from cu_q, not by batch
+  p.os_h = geo.os[1];
+  p.os_r = geo.os[2];
+  const long long items = static_cast<long long>(p.num_qtiles) * BH * p.num_splits;
+  p.num_items = static_cast<int>(items);
+  // persistent: one CTA per SM (shared and tensor memory allow no second), each walking
+  // its items
+  const int sms = sm_count(dev);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(items, sms > 0 ? sms : 1));
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));

@@ -70,7 +70,11 @@ struct FwdParams {
   const int32_t* cu_q;     // [B + 1] or null
   const int32_t* cu_k;     // [B + 1] or null
   int total_q, total_k;    // packed rows (the clamp for cu_q / cu_k)
-  __nv_bfloat16* o_packed; // packed sequences: O [total_q, H, D], for rows a TMA store would overrun
+  // O is stored straight from registers: element (b, h, row, x) at
+  // o + b * os_b + h * os_h + row * os_r + x (packed sequences: row counted from cu_q[0])
+  __nv_bfloat16* o;
+  long long os_b, os_h, os_r;
+  int num_items;           // work items: query tiles x splits
   // partial-state mode only: CTA (unit, split) absorbs key blocks [split * split_blocks,
   // (split + 1) * split_blocks) and writes the state (m, l, o~) instead of O and LSE
   int num_splits;          // >= 1
@@ -86,13 +90,18 @@ struct FwdCfg {
   static constexpr int kSubBytes = 128 * 128;         // 128 rows x 64 bf16 = 16 KiB
   static constexpr int kTileBytes = kSub * kSubBytes; // 128 rows x D bf16
   static constexpr int kStages = (D == 128) ? 3 : 4;  // K/V ring depth
+  // How a tile's O leaves (measured on GB300): at d = 64 it is staged in the V stage of the
+  // tile's last block and stored by TMA (a 16 KB tile in a 4-deep ring); at d = 128 the
+  // stage would take a third of the ring while the store reads it, so each thread stores
+  // its row straight from registers.
+  static constexpr bool kStageO = (D == 64);
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_full, k_full[S], v_full[S], k_free[S], v_free[S], s_full[3], pv_done[3],
-  // p_full[3], drain[2]
-  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kSBufs + 2;
+  // barriers: q_full, q_free, o_free, k_full[S], v_full[S], k_free[S], v_free[S],
+  // s_full[3], pv_done[3], p_full[3], drain[2]
+  static constexpr int kNumBars = 3 + 4 * kStages + 3 * kSBufs + 2;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack to align the base to 1024 B
@@ -142,8 +151,84 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// One work item = one 128-row query tile of one (batch, head), or, in partial-state
+// mode, one key split of such a tile.  decode() turns an item index into everything the
+// roles need about it; every role of the CTA decodes the same items in the same order.
+struct Item {
+  int bh, b, hh;           // (batch, head)
+  int q0;                  // first query row of the tile within its sequence
+  int q_base, k_base;      // first rows of the sequence in the Q / K maps
+  int Nq, Nk, bcoord;      // the sequence's lengths and its batch coordinate in the maps
+  int kv_len;              // visible keys after padding
+  int min_limit;           // smallest key limit of the tile's rows
+  int split, jb0, nblk;    // key blocks jb0 .. jb0 + nblk - 1 (nblk = 0: nothing to compute)
+  bool valid;              // false: a tile past the end of a shorter packed sequence
+};
+
+__device__ __forceinline__ Item decode(const FwdParams& p, int item) {
+  Item it;
+  const int nqt = p.num_qtiles;
+  it.split = item % p.num_splits;
+  const int unit = item / p.num_splits;
+  // heads in order (their K/V stay in L2 while their tiles run); within a head, causal
+  // tiles longest first
+  it.bh = unit / nqt;
+  int qtile = unit - it.bh * nqt;
+  if (p.causal) qtile = nqt - 1 - qtile;
+  it.b = it.bh / p.H;
+  it.hh = it.bh - it.b * p.H;
+  it.q0 = qtile * kBM;
+  it.q_base = 0;
+  it.k_base = 0;
+  it.Nq = p.Nq;
+  it.Nk = p.Nk;
+  it.bcoord = it.b;
+  it.valid = true;
+  if (p.cu_q) {
+    const int qs = min(max(__ldg(p.cu_q + it.b), 0), p.total_q);
+    const int qe = min(max(__ldg(p.cu_q + it.b + 1), qs), p.total_q);
+    const int ks = min(max(__ldg(p.cu_k + it.b), 0), p.total_k);
+    const int ke = min(max(__ldg(p.cu_k + it.b + 1), ks), p.total_k);
+    it.q_base = qs;
+    it.k_base = ks;
+    it.Nq = qe - qs;
+    it.Nk = ke - ks;
+    it.bcoord = 0;
+    it.valid = it.q0 < it.Nq;
+  }
+  it.kv_len = it.Nk;
+  if (p.lens) {
+    const int L = __ldg(p.lens + it.b);
+    it.kv_len = L < 0 ? 0 : (L > it.Nk ? it.Nk : L);
+  }
+  const int qlast = min(it.q0 + kBM - 1, it.Nq - 1);
+  const int max_limit = row_key_limit(qlast, it.kv_len, it.Nq, it.Nk, p.causal);
+  it.min_limit = row_key_limit(it.q0, it.kv_len, it.Nq, it.Nk, p.causal);
+  const int nvis = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;  // key blocks any row of the tile sees
+  // without splits an item takes every visible block (its key count may be per sequence)
+  it.jb0 = it.split * p.split_blocks;
+  const int nsplit = p.num_splits > 1 ? max(0, min(nvis, it.jb0 + p.split_blocks) - it.jb0) : nvis;
+  it.nblk = it.valid ? nsplit : 0;
+  return it;
+}
+
+// The items of CTA c, in order: round r takes items r G .. r G + G - 1 (G = number of
+// CTAs), forward in even rounds and backward in odd ones, so the long causal tiles at the
+// front of each head spread evenly over the CTAs.
+__device__ __forceinline__ int item_of(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
+
 // kSoftPairs: of every 16 pairs of scores in a block with no masked key, this many take
 // their exponential from exp2_poly2 instead of ex2.approx, to relieve the MUFU unit.
+//
+// The kernel is persistent: one CTA per SM walks its items.  The K/V ring, the score
+// buffers and their barriers run on without a break from one item to the next, so the
+// next tile's Q and first K/V blocks load and its first S product runs while the softmax
+// warps finish the previous tile.  Q is reused under q_free (the last S product of a tile
+// has read it); o~ is read out before the next tile's first P is handed over.  At d = 64 a
+// tile's O is staged (swizzled) in the shared-memory V stage of its last key block, whose
+// P V product has finished, and leaves by one TMA store; the softmax warps then hand that
+// stage back to the producer (v_free) instead of the P V issuer.  At d = 128 each thread
+// stores its row of O straight from registers.
 template <int D, bool kStates, int kSoftPairs>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -158,64 +243,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sV = sbase + C::kOffV;
   const uint32_t bar0 = sbase + C::kOffBar;
   const uint32_t bar_q_full = bar0;
-  auto bar_k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_v_full = [&](int s) { return bar0 + 8u * (1 + C::kStages + s); };
-  auto bar_k_free = [&](int s) { return bar0 + 8u * (1 + 2 * C::kStages + s); };
-  auto bar_v_free = [&](int s) { return bar0 + 8u * (1 + 3 * C::kStages + s); };
-  auto bar_s_full = [&](int b) { return bar0 + 8u * (1 + 4 * C::kStages + b); };
-  // pv_done[b] completes once per P_j V with j % 3 == b (it also frees score buffer b)
-  auto bar_pv_done = [&](int b) { return bar0 + 8u * (1 + 4 * C::kStages + kSBufs + b); };
-  // p_full[b]: the softmax warps have written P_j (and rescaled o~) for j % 3 == b
-  auto bar_p_full = [&](int b) { return bar0 + 8u * (1 + 4 * C::kStages + 2 * kSBufs + b); };
-  auto bar_drain = [&](int i) { return bar0 + 8u * (1 + 4 * C::kStages + 3 * kSBufs + i); };
+  const uint32_t bar_q_free = bar0 + 8u;   // the last S product of a tile has read Q
+  const uint32_t bar_o_free = bar0 + 16u;  // the softmax warps have read a tile's o~
+  auto bar_k_full = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto bar_v_full = [&](int s) { return bar0 + 8u * (3 + C::kStages + s); };
+  auto bar_k_free = [&](int s) { return bar0 + 8u * (3 + 2 * C::kStages + s); };
+  auto bar_v_free = [&](int s) { return bar0 + 8u * (3 + 3 * C::kStages + s); };
+  auto bar_s_full = [&](int b) { return bar0 + 8u * (3 + 4 * C::kStages + b); };
+  // pv_done[b] completes once per P_g V with g % 3 == b (it also frees score buffer b)
+  auto bar_pv_done = [&](int b) { return bar0 + 8u * (3 + 4 * C::kStages + kSBufs + b); };
+  // p_full[b]: the softmax warps have written P_g (and rescaled o~) for g % 3 == b
+  auto bar_p_full = [&](int b) { return bar0 + 8u * (3 + 4 * C::kStages + 2 * kSBufs + b); };
+  auto bar_drain = [&](int i) { return bar0 + 8u * (3 + 4 * C::kStages + 3 * kSBufs + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: heads in order (their K/V stay in L2 while their tiles run);
-  //      within a head, causal tiles longest first
-  const int nqt = p.num_qtiles;
-  const int split = kStates ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
-  const int unit = kStates ? static_cast<int>(blockIdx.x / p.num_splits) : static_cast<int>(blockIdx.x);
-  const int bh = unit / nqt;
-  int qtile = unit % nqt;
-  if (p.causal) qtile = nqt - 1 - qtile;
-  const int b = bh / p.H;
-  const int hh = bh - b * p.H;
-  const int q0 = qtile * kBM;
-  // this sequence: its first rows in the maps, its lengths, its batch coordinate
-  int q_base = 0, k_base = 0, Nq = p.Nq, Nk = p.Nk, bcoord = b;
-  if (p.cu_q) {
-    const int qs = min(max(__ldg(p.cu_q + b), 0), p.total_q);
-    const int qe = min(max(__ldg(p.cu_q + b + 1), qs), p.total_q);
-    const int ks = min(max(__ldg(p.cu_k + b), 0), p.total_k);
-    const int ke = min(max(__ldg(p.cu_k + b + 1), ks), p.total_k);
-    q_base = qs;
-    k_base = ks;
-    Nq = qe - qs;
-    Nk = ke - ks;
-    bcoord = 0;
-    if (q0 >= Nq) return;  // a tile past the end of a shorter sequence: nothing to do
-  }
-  int kv_len = Nk;
-  if (p.lens) {
-    const int L = __ldg(p.lens + b);
-    kv_len = L < 0 ? 0 : (L > Nk ? Nk : L);
-  }
-  const int qlast = min(q0 + kBM - 1, Nq - 1);
-  const int max_limit = row_key_limit(qlast, kv_len, Nq, Nk, p.causal);
-  const int min_limit = row_key_limit(q0, kv_len, Nq, Nk, p.causal);
-  const int nvis = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;  // key blocks any row of the tile sees
-  // this CTA absorbs key blocks jb0 .. jb0 + nblk - 1 (all of them unless it computes one split)
-  const int jb0 = kStates ? split * p.split_blocks : 0;
-  const int nblk = kStates ? max(0, min(nvis, jb0 + p.split_blocks) - jb0) : nvis;
-
+  const int G = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
   WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_free, 1);
+    mbar_init(bar_o_free, 4);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_k_full(s), 1);
       mbar_init(bar_v_full(s), 1);
@@ -237,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmO);
+    if (!kStates && C::kStageO) tma_prefetch_desc(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -246,88 +298,132 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     // ================================================================ producer
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       const uint64_t pol_kv = policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
-      mbar_arrive_expect_tx(bar_q_full, C::kTileBytes);
-      for (int s = 0; s < C::kSub; ++s)
-        tma_load_4d(sQ + s * C::kSubBytes, &tmQ, bar_q_full, s * 64, q_base + q0, hh, bcoord, pol_q);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nblk; ++j) {
-        const int st = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
-        if (!mbar_wait(bar_k_free(st), ph ^ 1, wc, 1)) break;
-        if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
-          mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_4d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64,
-                        k_base + (jb0 + j) * kBN, hh, bcoord, pol_kv);
-        }
-        k_issued = j + 1;
-        if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) break;
-        mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
+      int g = 0;   // key blocks loaded so far over all items: ring slot g % kStages
+      int kq = 0;  // items with work so far: uses of the Q buffer
+      int k_last[C::kStages], v_last[C::kStages];  // last load issued into each stage (-1: none)
+      for (int s = 0; s < C::kStages; ++s) k_last[s] = v_last[s] = -1;
+      bool ok = true;
+      for (int ri = 0; ok; ++ri) {
+        const int item = item_of(ri, cta, G);
+        if (item >= p.num_items) break;
+        const Item it = decode(p, item);
+        if (it.nblk == 0) continue;
+        // the previous tile's Q must have been read by its last S product
+        if (kq > 0 && !mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13)) break;
+        mbar_arrive_expect_tx(bar_q_full, C::kTileBytes);
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_4d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64,
-                      k_base + (jb0 + j) * kBN, hh, bcoord, pol_kv);
-        v_issued = j + 1;
+          tma_load_4d(sQ + s * C::kSubBytes, &tmQ, bar_q_full, s * 64, it.q_base + it.q0, it.hh, it.bcoord, pol_q);
+        ++kq;
+        for (int j = 0; j < it.nblk; ++j, ++g) {
+          const int st = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          if (!mbar_wait(bar_k_free(st), ph ^ 1, wc, 1)) {
+            ok = false;
+            break;
+          }
+          k_last[st] = -1;
+          if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
+            mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
+            for (int s = 0; s < C::kSub; ++s)
+              tma_load_4d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64,
+                          it.k_base + (it.jb0 + j) * kBN, it.hh, it.bcoord, pol_kv);
+            k_last[st] = g;
+          }
+          if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_4d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64,
+                        it.k_base + (it.jb0 + j) * kBN, it.hh, it.bcoord, pol_kv);
+          v_last[st] = g;
+        }
       }
-      // Let the last copies issued land before this warp leaves (in a normal run they were
-      // consumed long ago; after a failed wait nobody else will wait for them).
-      for (int i = (k_issued > C::kStages ? k_issued - C::kStages : 0); i < k_issued; ++i)
-        if (i != p.fault_block) mbar_wait_drain(bar_k_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
-      for (int i = (v_issued > C::kStages ? v_issued - C::kStages : 0); i < v_issued; ++i)
-        mbar_wait_drain(bar_v_full(i % C::kStages), (i / C::kStages) & 1, p.timeout_ns);
+      // Let the copies still in flight land before this warp leaves (in a normal run they
+      // were consumed long ago; after a failed wait nobody else will wait for them).
+      for (int s = 0; s < C::kStages; ++s) {
+        if (k_last[s] >= 0) mbar_wait_drain(bar_k_full(s), (k_last[s] / C::kStages) & 1, p.timeout_ns);
+        if (v_last[s] >= 0) mbar_wait_drain(bar_v_full(s), (v_last[s] / C::kStages) & 1, p.timeout_ns);
+      }
     }
   } else if (warp == kWarpPv || warp == kWarpS) {
     // ================================================================ MMA issuers
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       // Shared-memory descriptors: the high word (stride 1024 B, version 1, 128-byte
       // swizzle) is the same for every operand; the low word holds the start address
       // (>> 4) and the leading byte offset, so a k-step is one add to the low word.
       const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      int g = 0;   // key blocks over all items
+      int kq = 0;  // items with work
       bool ok = true;
       if (warp == kWarpS) {
         const uint32_t qlo = (sQ >> 4) | (1u << 16);
         const uint32_t klo = (sK >> 4) | (1u << 16);
-        ok = mbar_wait(bar_q_full, 0, wc, 3);
-        for (int j = 0; ok && j < nblk; ++j) {
-          const int st = j % C::kStages;
-          const int bf = j % kSBufs;
-          // buffer bf last held P_{j-3}: its P V product must have consumed it
-          if (j >= kSBufs) ok = mbar_wait(bar_pv_done(bf), ((j - kSBufs) / kSBufs) & 1, wc, 4);
-          ok = ok && mbar_wait(bar_k_full(st), (j / C::kStages) & 1, wc, 5);
-          if (!ok) break;
-          tc_fence_after();
-          // S_j = Q K_j^T: 8 (d = 128) or 4 (d = 64) k-steps of 16
-          const uint32_t blo = klo + st * (C::kTileBytes >> 4);
-          const uint32_t d = tmem + C::col_s(bf);
+        for (int ri = 0; ok; ++ri) {
+          const int item = item_of(ri, cta, G);
+          if (item >= p.num_items) break;
+          const Item it = decode(p, item);
+          if (it.nblk == 0) continue;
+          ok = mbar_wait(bar_q_full, kq & 1, wc, 3);
+          for (int j = 0; ok && j < it.nblk; ++j, ++g) {
+            const int st = g % C::kStages;
+            const int bf = g % kSBufs;
+            // buffer bf last held P_{g-3}: its P V product must have consumed it
+            if (g >= kSBufs) ok = mbar_wait(bar_pv_done(bf), ((g - kSBufs) / kSBufs) & 1, wc, 4);
+            ok = ok && mbar_wait(bar_k_full(st), (g / C::kStages) & 1, wc, 5);
+            if (!ok) break;
+            tc_fence_after();
+            // S_g = Q K_g^T: 8 (d = 128) or 4 (d = 64) k-steps of 16
+            const uint32_t blo = klo + st * (C::kTileBytes >> 4);
+            const uint32_t dst = tmem + C::col_s(bf);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks / 4) * (C::kSubBytes >> 4) + (ks % 4) * 2;
-            mma_ss(d, (static_cast<uint64_t>(dhi) << 32) | (qlo + off),
-                   (static_cast<uint64_t>(dhi) << 32) | (blo + off), C::kIdescS, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks / 4) * (C::kSubBytes >> 4) + (ks % 4) * 2;
+              mma_ss(dst, (static_cast<uint64_t>(dhi) << 32) | (qlo + off),
+                     (static_cast<uint64_t>(dhi) << 32) | (blo + off), C::kIdescS, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(bar_s_full(bf));
+            mma_commit(bar_k_free(st));
           }
-          mma_commit(bar_s_full(bf));
-          mma_commit(bar_k_free(st));
+          if (!ok) break;
+          mma_commit(bar_q_free);  // Q may be overwritten once this tile's products have read it
+          ++kq;
         }
       } else {
         const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
-        for (int j = 0; ok && j < nblk; ++j) {
-          const int st = j % C::kStages;
-          // V_j has normally landed long before P_j is ready: check it first
-          ok = mbar_wait(bar_v_full(st), (j / C::kStages) & 1, wc, 7) &&
-               mbar_wait_poll(bar_p_full(j % kSBufs), (j / kSBufs) & 1, wc, 6);
-          if (!ok) break;
-          tc_fence_after();
-          // o~ += P_j V_j: 8 k-steps of 16 keys; A = P_j from tensor memory, B = V_j MN-major
-          const uint32_t blo = vlo + st * (C::kTileBytes >> 4);
-          const uint32_t a = tmem + C::col_s(j % kSBufs);
+        for (int ri = 0; ok; ++ri) {
+          const int item = item_of(ri, cta, G);
+          if (item >= p.num_items) break;
+          const Item it = decode(p, item);
+          if (it.nblk == 0) continue;
+          // The first product of a tile overwrites o~.  The softmax warps read the previous
+          // tile's o~ out before they write this tile's first P, and P_0 is awaited below,
+          // so that ordering needs no barrier of its own.
+          for (int j = 0; ok && j < it.nblk; ++j, ++g) {
+            const int st = g % C::kStages;
+            // V_g has normally landed long before P_g is ready: check it first
+            ok = mbar_wait(bar_v_full(st), (g / C::kStages) & 1, wc, 7) &&
+                 mbar_wait_poll(bar_p_full(g % kSBufs), (g / kSBufs) & 1, wc, 6);
+            if (!ok) break;
+            tc_fence_after();
+            // o~ += P_g V_g: 8 k-steps of 16 keys; A = P_g from tensor memory, B = V_g MN-major
+            const uint32_t blo = vlo + st * (C::kTileBytes >> 4);
+            const uint32_t a = tmem + C::col_s(g % kSBufs);
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_ts(tmem + C::kColO, a + ks * 8, (static_cast<uint64_t>(dhi) << 32) | (blo + ks * (16 * 128 >> 4)),
-                   C::kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(bar_pv_done(j % kSBufs));
-          mma_commit(bar_v_free(st));
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              mma_ts(tmem + C::kColO, a + ks * 8,
+                     (static_cast<uint64_t>(dhi) << 32) | (blo + ks * (16 * 128 >> 4)), C::kIdescO,
+                     (j > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(bar_pv_done(g % kSBufs));
+            // The V stage of a tile's last block is handed back by the softmax warps instead:
+            // they stage the tile's O in it for the TMA store
+            if (kStates || !C::kStageO || j + 1 < it.nblk) mma_commit(bar_v_free(st));
+          }
+          ++kq;
         }
       }
       // every MMA this thread issued must finish before tensor memory is released (in a
@@ -337,140 +433,210 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ softmax / epilogue
-    const int r = threadIdx.x;             // 0..127: row within the tile = tensor-memory lane
-    const int row = q0 + r;
-    const int limit = row_key_limit(row, kv_len, Nq, Nk, p.causal);
+    const int r = threadIdx.x;  // 0..127: row within the tile = tensor-memory lane
     const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float c = p.c;
-    float m = -INFINITY;  // running max, log2 domain
-    float l = 0.f;        // running denominator
+    int g = 0;  // key blocks over all items: score buffer g % 3
     bool ok = true;
-    // Checking a barrier costs a long round trip even when its phase completed long ago.
-    // The two checks of every block are therefore issued early, as non-blocking tests
-    // whose results are consumed later: s_full of the next block during this block's
-    // exponentials, pv_done of the previous block before their last chunk.  Only when a test
-    // says "not yet" does the thread take the (bounded) wait.
-    bool s_seen = false;  // s_full of block j already seen complete
-    for (int j = 0; j < nblk; ++j) {
-      const uint32_t colS = C::col_s(j % kSBufs);
-      // every lane of the warp takes the same branch: the tcgen05 loads below are warp-wide
-      if (!__all_sync(0xffffffffu, s_seen))
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(j % kSBufs), (j / kSBufs) & 1, wc, 9));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[kBN];
-#pragma unroll
-      for (int q = 0; q < kBN / 32; ++q) tmem_ld32(tl + colS + q * 32, sr + q * 32);
-      tmem_wait_ld();
-      float s[kBN];
-#pragma unroll
-      for (int k = 0; k < kBN; ++k) s[k] = __uint_as_float(sr[k]);
-      const int kb = (jb0 + j) * kBN;
-      if (kb + kBN > min_limit) {
-#pragma unroll
-        for (int k = 0; k < kBN; ++k)
-          if (kb + k >= limit) s[k] = -INFINITY;
-      }
-      // block max: eight independent chains of 3-input max over s[0..kBN)
-      float a[8];
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmaxf(s[2 * c8], s[2 * c8 + 1]);
-#pragma unroll
-      for (int k = 16; k < kBN; k += 16) {
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmax3(a[c8], s[k + 2 * c8], s[k + 2 * c8 + 1]);
-      }
-      const float mx = fmaxf(fmaxf(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5])), fmaxf(a[6], a[7]));
-      // the reference moves when the block max passes it by more than tau (tau = 0: whenever
-      // the max rises, the pages' rule; a row that has seen no visible key stays at -inf)
-      const float mb = mx * c;
-      const float m_new = (mb > m + p.tau) ? mb : m;
-      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_ref);
-      // p = exp2(c*s - m_ref), summed in fp32, packed to bf16 and stored 32 keys at a time
-      const float2 c2 = make_float2(c, c);
-      const float2 nm2 = make_float2(-m_ref, -m_ref);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      bool pv_seen = false;  // pv_done of block j - 1 seen complete
-      auto exp_block = [&](auto soft_tag) {
-        constexpr bool kSoft = decltype(soft_tag)::value;
-#pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) {
-          if (q == 0)
-            s_seen = j + 1 < nblk && mbar_test_wait(bar_s_full((j + 1) % kSBufs), ((j + 1) / kSBufs) & 1);
-          if (q == 3)
-            pv_seen = j > 0 && mbar_test_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1);
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float2 x = __ffma2_rn(make_float2(s[q * 32 + 2 * k], s[q * 32 + 2 * k + 1]), c2, nm2);
-            if (kSoft && (k * kSoftPairs) % 16 < kSoftPairs) {
-              x = exp2_poly2(x);
-            } else {
-              x.x = ex2_approx(x.x);
-              x.y = ex2_approx(x.y);
-            }
-            if (k & 1)
-              acc1 = __fadd2_rn(acc1, x);
-            else
-              acc0 = __fadd2_rn(acc0, x);
-            pk[k] = pack_bf16x2(x.x, x.y);
-          }
-          tmem_st16(tl + colS + q * 16, pk);
-        }
-      };
-      // blocks with a masked key (-inf scores) keep every exponential on ex2.approx
-      if (kSoftPairs > 0 && kb + kBN <= min_limit)
-        exp_block(std::true_type{});
-      else
-        exp_block(std::false_type{});
-      const float2 acc = __fadd2_rn(acc0, acc1);
-      l = l * alpha + (acc.x + acc.y);
-      m = m_new;
-      if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
-        // o~ may be touched only after the previous P V product has landed in it
-        if (!__all_sync(0xffffffffu, pv_seen))
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(bar_pv_done((j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, wc, 10));
+    for (int ri = 0; ok; ++ri) {
+      const int item = item_of(ri, cta, G);
+      if (item >= p.num_items) break;
+      const Item it = decode(p, item);
+      if (!it.valid) continue;  // a tile past the end of a shorter packed sequence
+      const int row = it.q0 + r;
+      const int limit = row_key_limit(row, it.kv_len, it.Nq, it.Nk, p.causal);
+      const int nblk = it.nblk;
+      float m = -INFINITY;  // running max, log2 domain
+      float l = 0.f;        // running denominator
+      // Checking a barrier costs a long round trip even when its phase completed long ago.
+      // The two checks of every block are therefore issued early, as non-blocking tests
+      // whose results are consumed later: s_full of the next block during this block's
+      // exponentials, pv_done of the previous block before their last chunk.  Only when a
+      // test says "not yet" does the thread take the (bounded) wait.
+      bool s_seen = false;  // s_full of block j already seen complete
+      for (int j = 0; j < nblk; ++j) {
+        const int gj = g + j;  // this block's index over all items
+        const uint32_t colS = C::col_s(gj % kSBufs);
+        // every lane of the warp takes the same branch: the tcgen05 loads below are warp-wide
+        if (!__all_sync(0xffffffffu, s_seen))
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_s_full(gj % kSBufs), (gj / kSBufs) & 1, wc, 9));
         if (!ok) break;
         tc_fence_after();
-        const float2 al2 = make_float2(alpha, alpha);
+        uint32_t sr[kBN];
 #pragma unroll
-        for (int q = 0; q < D / 64; ++q) {
-          uint32_t o[64];
-          tmem_ld32(tl + C::kColO + q * 64, o);
-          tmem_ld32(tl + C::kColO + q * 64 + 32, o + 32);
+        for (int q = 0; q < kBN / 32; ++q) tmem_ld32(tl + colS + q * 32, sr + q * 32);
+        tmem_wait_ld();
+        float s[kBN];
+#pragma unroll
+        for (int k = 0; k < kBN; ++k) s[k] = __uint_as_float(sr[k]);
+        const int kb = (it.jb0 + j) * kBN;
+        if (kb + kBN > it.min_limit) {
+#pragma unroll
+          for (int k = 0; k < kBN; ++k)
+            if (kb + k >= limit) s[k] = -INFINITY;
+        }
+        // block max: eight independent chains of 3-input max over s[0..kBN)
+        float a[8];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmaxf(s[2 * c8], s[2 * c8 + 1]);
+#pragma unroll
+        for (int k = 16; k < kBN; k += 16) {
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) a[c8] = fmax3(a[c8], s[k + 2 * c8], s[k + 2 * c8 + 1]);
+        }
+        const float mx = fmaxf(fmaxf(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5])), fmaxf(a[6], a[7]));
+        // the reference moves when the block max passes it by more than tau (tau = 0:
+        // whenever the max rises, the pages' rule; a row that has seen no visible key stays
+        // at -inf)
+        const float mb = mx * c;
+        const float m_new = (mb > m + p.tau) ? mb : m;
+        const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2_approx(m - m_ref);
+        // p = exp2(c*s - m_ref), summed in fp32, packed to bf16 and stored 32 keys at a time
+        const float2 c2 = make_float2(c, c);
+        const float2 nm2 = make_float2(-m_ref, -m_ref);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        bool pv_seen = false;  // pv_done of block j - 1 seen complete
+        auto exp_block = [&](auto soft_tag) {
+          constexpr bool kSoft = decltype(soft_tag)::value;
+#pragma unroll
+          for (int q = 0; q < kBN / 32; ++q) {
+            if (q == 0)
+              s_seen = j + 1 < nblk && mbar_test_wait(bar_s_full((gj + 1) % kSBufs), ((gj + 1) / kSBufs) & 1);
+            if (q == 3)
+              pv_seen = j > 0 && mbar_test_wait(bar_pv_done((gj - 1) % kSBufs), ((gj - 1) / kSBufs) & 1);
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              float2 x = __ffma2_rn(make_float2(s[q * 32 + 2 * k], s[q * 32 + 2 * k + 1]), c2, nm2);
+              if (kSoft && (k * kSoftPairs) % 16 < kSoftPairs) {
+                x = exp2_poly2(x);
+              } else {
+                x.x = ex2_approx(x.x);
+                x.y = ex2_approx(x.y);
+              }
+              if (k & 1)
+                acc1 = __fadd2_rn(acc1, x);
+              else
+                acc0 = __fadd2_rn(acc0, x);
+              pk[k] = pack_bf16x2(x.x, x.y);
+            }
+            tmem_st16(tl + colS + q * 16, pk);
+          }
+        };
+        // blocks with a masked key (-inf scores) keep every exponential on ex2.approx
+        if (kSoftPairs > 0 && kb + kBN <= it.min_limit)
+          exp_block(std::true_type{});
+        else
+          exp_block(std::false_type{});
+        const float2 acc = __fadd2_rn(acc0, acc1);
+        l = l * alpha + (acc.x + acc.y);
+        m = m_new;
+        if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.f)) {
+          // o~ may be touched only after the previous P V product has landed in it
+          if (!__all_sync(0xffffffffu, pv_seen))
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar_pv_done((gj - 1) % kSBufs), ((gj - 1) / kSBufs) & 1, wc, 10));
+          if (!ok) break;
+          tc_fence_after();
+          const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int q = 0; q < D / 64; ++q) {
+            uint32_t o[64];
+            tmem_ld32(tl + C::kColO + q * 64, o);
+            tmem_ld32(tl + C::kColO + q * 64 + 32, o + 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2);
+              o[2 * k] = __float_as_uint(v.x);
+              o[2 * k + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tl + C::kColO + q * 64, o);
+            tmem_st32(tl + C::kColO + q * 64 + 32, o + 32);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p_full(gj % kSBufs));
+      }
+      // ---- epilogue: one division by l; O and LSE out
+      const int gl = g + nblk - 1;  // the tile's last block
+      if (ok && nblk > 0) {
+        // the last P V (also the last MMA of the tile) has landed in o~
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv_done(gl % kSBufs), (gl / kSBufs) & 1, wc, 11));
+        tc_fence_after();
+      }
+      g += nblk;
+      const bool store = row < it.Nq;
+      if (!kStates && C::kStageO && nblk > 0) {
+        // O through the V stage of the last block and one TMA store.  Every softmax warp
+        // reaches this barrier once per tile with blocks, also after a failed wait (it left
+        // the block loop early), so they all agree on giving up and leave together.
+        const bool give_up = bar_sync_or(1, 128, !ok || *abort_flag != 0u);
+        if (give_up) {
+          ok = false;
+          break;
+        }
+        const int st_last = gl % C::kStages;
+        const uint32_t stage = sV + st_last * C::kTileBytes;
+        uint8_t* orow = smem + (stage - sbase) + r * 128;
+        // the last tile of a packed sequence would overrun into the next sequence under a
+        // TMA store: its rows are stored one by one instead (the same for the whole CTA)
+        const bool direct = p.cu_q != nullptr && it.q0 + kBM > it.Nq;
+        uint4* gdst = reinterpret_cast<uint4*>(p.o + it.b * p.os_b + it.hh * p.os_h +
+                                               (it.q_base + (store ? row : 0)) * p.os_r);
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tl + C::kColO + q * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            float2 v = __fmul2_rn(make_float2(__uint_as_float(o[2 * k]), __uint_as_float(o[2 * k + 1])), al2);
-            o[2 * k] = __float_as_uint(v.x);
-            o[2 * k + 1] = __float_as_uint(v.y);
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * inv, __uint_as_float(o[ch * 8 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * inv, __uint_as_float(o[ch * 8 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv, __uint_as_float(o[ch * 8 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv, __uint_as_float(o[ch * 8 + 7]) * inv);
+            if (direct) {
+              if (store) gdst[q * 4 + ch] = v;
+            } else {
+              // columns 32q .. 32q + 31 = four 16-byte chunks of sub-tile q / 2, chunk
+              // (q % 2) * 4 + ch, 128-byte swizzle
+              const int chunk = (q % 2) * 4 + ch;
+              *reinterpret_cast<uint4*>(orow + (q / 2) * C::kSubBytes + ((chunk ^ (r & 7)) * 16)) = v;
+            }
           }
-          tmem_st32(tl + C::kColO + q * 64, o);
-          tmem_st32(tl + C::kColO + q * 64 + 32, o + 32);
         }
+        if (store) {
+          const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          const size_t li = p.cu_q ? static_cast<size_t>(it.hh) * p.total_q + it.q_base + row
+                                   : static_cast<size_t>(it.bh) * p.Nq + row;
+          p.lse[li] = lse;
+        }
+        fence_proxy_async_smem();
+        bar_sync_named(1, 128);
+        if (r == 0) {
+          if (!direct) {
+            for (int s = 0; s < C::kSub; ++s)
+              tma_store_4d(&tmO, stage + s * C::kSubBytes, s * 64, it.q_base + it.q0, it.hh, it.bcoord);
+            tma_store_commit();
+            tma_store_wait_read();  // the stage may be loaded again once the store has read it
+          }
+          mbar_arrive(bar_v_free(st_last));
+        }
+        // o~ has been read out (tcgen05 loads waited above): the next tile's first P V
+        // product, ordered after this thread's next arrival on p_full, may overwrite it
+        tc_fence_before();
+        continue;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full(j % kSBufs));
-    }
-    // ---- epilogue: one division by l, O through shared memory and a TMA store, LSE direct
-    if (ok && nblk > 0) {
-      // the last P V (also the last MMA of the tile) has landed in o~
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(bar_pv_done((nblk - 1) % kSBufs), ((nblk - 1) / kSBufs) & 1, wc, 11));
-      tc_fence_after();
-    }
-    // one decision for all four softmax warps (the named barriers below need all of them)
-    const bool give_up = bar_sync_or(1, 128, !ok || *abort_flag != 0u);
-    if constexpr (kStates) {
-      // the state of this split, undivided: o~ and l as accumulated, m back in natural-log
-      // units of the scaled scores (m2 = c * max q.k, c = scale * log2 e, so m = m2 * ln 2)
-      if (!give_up) {
-        const bool store = row < p.Nq;
-        const size_t ridx = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + (store ? row : 0);
+      if (!ok) break;
+      if constexpr (kStates) {
+        // the state of this split, undivided: o~ and l as accumulated, m back in natural-log
+        // units of the scaled scores (m2 = c * max q.k, c = scale * log2 e, so m = m2 * ln 2)
+        const size_t ridx = (static_cast<size_t>(it.split) * p.BH + it.bh) * p.Nq + (store ? row : 0);
         float4* dst = reinterpret_cast<float4*>(p.st_o + ridx * D);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -493,62 +659,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.st_m[ridx] = m * 0.69314718055994531f;  // -inf stays -inf for a row that saw no key
           p.st_l[ridx] = l;
         }
-      }
-    } else if (!give_up) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t* orow = smem + C::kOffQ + r * 128;
-      // The tile goes out by one TMA store, which clips rows past the end of the map.  The
-      // last tile of a packed sequence would overrun into the next sequence: its rows are
-      // stored one by one instead (the same for the whole CTA).
-      const bool direct = p.cu_q != nullptr && q0 + kBM > Nq;
-      uint4* grow = direct ? reinterpret_cast<uint4*>(p.o_packed + (static_cast<size_t>(q_base + min(row, Nq - 1)) *
-                                                                         p.H + hh) * D)
-                           : nullptr;
+      } else {  // straight from registers (d = 128, or a tile with no visible key)
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + it.b * p.os_b + it.hh * p.os_h +
+                                              (it.q_base + (store ? row : 0)) * p.os_r);
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t o[32];
-        if (nblk > 0) {
-          tmem_ld32(tl + C::kColO + q * 32, o);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0u;
-        }
-        // 32 columns = four 16-byte chunks of sub-tile q/2, chunk (q%2)*4 + ch, 128-byte swizzle
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * inv, __uint_as_float(o[ch * 8 + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * inv, __uint_as_float(o[ch * 8 + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv, __uint_as_float(o[ch * 8 + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv, __uint_as_float(o[ch * 8 + 7]) * inv);
-          const int chunk = (q % 2) * 4 + ch;
-          if (direct) {
-            if (row < Nq) grow[q * 4 + ch] = v;
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          if (nblk > 0) {  // warp-wide load: every lane takes part, tail rows then skip the store
+            tmem_ld32(tl + C::kColO + q * 32, o);
+            tmem_wait_ld();
           } else {
-            *reinterpret_cast<uint4*>(orow + (q / 2) * C::kSubBytes + ((chunk ^ (r & 7)) * 16)) = v;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = 0u;
+          }
+          if (store) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[ch * 8 + 0]) * inv, __uint_as_float(o[ch * 8 + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(o[ch * 8 + 2]) * inv, __uint_as_float(o[ch * 8 + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(o[ch * 8 + 4]) * inv, __uint_as_float(o[ch * 8 + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(o[ch * 8 + 6]) * inv, __uint_as_float(o[ch * 8 + 7]) * inv);
+              dst[q * 4 + ch] = v;
+            }
           }
         }
-      }
-      if (row < Nq) {
-        const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-        // [B, H, Nq], or [H, total_q] for packed sequences
-        const size_t li = p.cu_q ? static_cast<size_t>(hh) * p.total_q + q_base + row
-                                 : static_cast<size_t>(bh) * p.Nq + row;
-        p.lse[li] = lse;
-      }
-      if (!direct) {
-        fence_proxy_async_smem();
-        bar_sync_named(1, 128);
-        if (r == 0) {
-          for (int s = 0; s < C::kSub; ++s) tma_store_4d(&tmO, sQ + s * C::kSubBytes, s * 64, q_base + q0, hh, bcoord);
-          tma_store_commit();
-          tma_store_wait_all();
+        if (store) {
+          const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          // [B, H, Nq], or [H, total_q] for packed sequences
+          const size_t li = p.cu_q ? static_cast<size_t>(it.hh) * p.total_q + it.q_base + row
+                                   : static_cast<size_t>(it.bh) * p.Nq + row;
+          p.lse[li] = lse;
         }
       }
+      // o~ has been read out (tcgen05 loads waited above): the next tile's first P V product,
+      // ordered after this thread's next arrival on p_full, may overwrite it
+      tc_fence_before();
     }
   }
 
+  if (!kStates && C::kStageO && threadIdx.x == 0) tma_store_wait_all();  // the last O tile is out
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpPv) {
