@@ -1,12 +1,13 @@
 // Fused attention forward with the online-softmax recurrence, sm_103a.
 //
-// One CTA computes one tile of 128 query rows of one (batch, head).  Warp roles:
+// A CTA computes tiles of 128 query rows of one (batch, head) at a time (persistently:
+// one CTA per SM walks its tiles, see attn_fwd_kernel below).  Warp roles:
 //   warps 0-3  softmax: thread r owns query row r of the tile (tensor-memory lane r).
 //              Per key block it reads the score row S from tensor memory, masks, takes
 //              the block max, computes alpha and p = exp2(c*s - m), updates l, writes P
 //              (bf16) back into tensor memory over its own S and rescales the output
 //              accumulator o~ by alpha when some row of its warp saw the max rise.  At the
-//              end it divides o~ by l once and writes O (TMA store) and LSE.
+//              end it divides o~ by l once and writes O and LSE.
 //   warp 4     producer: TMA loads of the Q tile and of K/V blocks into a ring of
 //              shared-memory stages guarded by full/free mbarriers.
 //   warp 5     P V issuer: tcgen05.mma o~ += P_j V_j (P from tensor memory, V from shared
@@ -99,8 +100,8 @@ struct FwdCfg {
   static constexpr int kOffK = kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_full, q_free, o_free, k_full[S], v_full[S], k_free[S], v_free[S],
-  // s_full[3], pv_done[3], p_full[3], drain[2]
+  // barriers: q_full, q_free, (one unused slot), k_full[S], v_full[S], k_free[S],
+  // v_free[S], s_full[3], pv_done[3], p_full[3], drain[2]
   static constexpr int kNumBars = 3 + 4 * kStages + 3 * kSBufs + 2;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16;
@@ -244,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + C::kOffBar;
   const uint32_t bar_q_full = bar0;
   const uint32_t bar_q_free = bar0 + 8u;   // the last S product of a tile has read Q
-  const uint32_t bar_o_free = bar0 + 16u;  // the softmax warps have read a tile's o~
   auto bar_k_full = [&](int s) { return bar0 + 8u * (3 + s); };
   auto bar_v_full = [&](int s) { return bar0 + 8u * (3 + C::kStages + s); };
   auto bar_k_free = [&](int s) { return bar0 + 8u * (3 + 2 * C::kStages + s); };
@@ -267,7 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     mbar_init(bar_q_free, 1);
-    mbar_init(bar_o_free, 4);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar_k_full(s), 1);
       mbar_init(bar_v_full(s), 1);
