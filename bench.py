@@ -79,10 +79,17 @@ def host_cores() -> int:
 
 
 def kernel_source_hash() -> str:
+    """Identifies the kernel code a profile was taken on: the sources with comments and
+    blank lines removed, so editing a comment does not void a recorded profile."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "online_softmax_flashattention_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "online_softmax_flashattention_attention_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 
