@@ -1,0 +1,98 @@
+"""The persistent kernel with several items per CTA, compared whole with the oracle.
+
+The kernel runs one CTA per SM, each walking its items (query tiles, or tiles x key
+splits) in a snake order, with the K/V ring, the score buffers and their barrier phases
+carried from one item to the next.  The shapes here have two to six times as many
+items as the GPU has SMs, mixed with items that have no visible key (fully masked
+batches), tail tiles and short sequences, so every CTA crosses several item boundaries.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from gpu_helpers import compare, run_cuda, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def custom(B, H, Nq, Nk, d, causal=False, seed=7, lens=None):
+    w = dict(name="custom", B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=causal, qk=("normal", 0.0, 1.0),
+             v=("normal", 0.0, 1.0), seed=seed, lens=None if lens is None else ("given", lens), plant=None,
+             scale=1.0 / math.sqrt(d))
+    return gen.make_inputs(w)
+
+
+def sms():
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+CASES = [
+    # B, H, Nq, Nk, d, causal, lens               items = B * H * ceil(Nq / 128)
+    (4, 40, 300, 300, 128, True, None),           # 480
+    (4, 30, 300, 450, 64, False, [450, 0, 129, 0]),  # 360, half of them with no visible key
+    (6, 20, 260, 260, 128, False, [1, 260, 0, 77, 200, 129]),  # 360
+    (2, 64, 200, 600, 128, True, None),           # 256, Nq < Nk (bottom-right causal)
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,lens", CASES)
+def test_many_items_per_cta(B, H, Nq, Nk, d, causal, lens):
+    items = B * H * -(-Nq // 128)
+    assert items > sms(), "the case must give CTAs more than one item"
+    x = custom(B, H, Nq, Nk, d, causal, seed=900 + B * H + Nq, lens=lens)
+    O, LSE = run_cuda(x)
+    O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"])
+    compare(O, LSE, O_ref, LSE_ref)
+
+
+def test_many_items_split_states():
+    """Split-KV states with more (tile, split) items than SMs."""
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    B, H, Nq, Nk, d, S = 2, 40, 256, 900, 128, 3     # 2 * 40 * 2 * 3 = 480 items
+    x = custom(B, H, Nq, Nk, d, True, seed=77, lens=[900, 500])
+    lt = torch.as_tensor(np.asarray(x["lens"], np.int32)).cuda()
+    O, LSE = pkg.attn_fwd_splitkv(to_device(x["Q"]), to_device(x["K"]), to_device(x["V"]), num_splits=S,
+                                  scale=x["scale"], causal=True, key_padding_lens=lt)
+    pkg.status_sync()
+    O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], True, x["lens"])
+    compare(O.float().cpu().numpy().astype(np.float64), LSE.cpu().numpy().astype(np.float64), O_ref, LSE_ref)
+
+
+def test_many_packed_sequences():
+    """Packed sequences: 70 of them, 3 heads, lengths 0..400: several items per CTA, many
+    of them past the end of their (shorter) sequence."""
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    rng = np.random.default_rng(5)
+    H, d = 3, 128
+    lq = rng.integers(0, 400, size=70)
+    lk = lq + rng.integers(0, 200, size=70)
+    total_q, total_k = int(lq.sum()), int(lk.sum())
+    w = dict(name="packed", B=1, H=H, Nq=total_q, Nk=total_k, d=d, causal=False, qk=("normal", 0.0, 1.0),
+             v=("normal", 0.0, 1.0), seed=31, lens=None, plant=None, scale=1.0 / math.sqrt(d))
+    x = gen.make_inputs(w)
+    Qp = np.ascontiguousarray(x["Q"][0].transpose(1, 0, 2))   # [total_q, H, d]
+    Kp = np.ascontiguousarray(x["K"][0].transpose(1, 0, 2))
+    Vp = np.ascontiguousarray(x["V"][0].transpose(1, 0, 2))
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    O, LSE = pkg.attn_fwd_varlen(to_device(Qp), to_device(Kp), to_device(Vp), torch.from_numpy(cu_q).cuda(),
+                                 torch.from_numpy(cu_k).cuda(), int(lq.max()), scale=x["scale"], causal=True)
+    pkg.status_sync()
+    Of = O.float().cpu().numpy().astype(np.float64)
+    Lf = LSE.cpu().numpy().astype(np.float64)
+    for b in range(70):
+        if lq[b] == 0:
+            continue
+        rq, rk = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
+        O_ref = np.zeros((H, lq[b], d))
+        L_ref = np.zeros((H, lq[b]))
+        for h in range(H):
+            O_ref[h], L_ref[h] = oracle.attention_head(oracle.bf16_to_f64(Qp[rq, h]), oracle.bf16_to_f64(Kp[rk, h]),
+                                                       oracle.bf16_to_f64(Vp[rk, h]), x["scale"], True)
+        compare(Of[rq].transpose(1, 0, 2), Lf[:, rq], O_ref, L_ref)
