@@ -41,7 +41,7 @@ METRIC = "attention fwd TFLOP/s (bf16, d=128) and % of GB300 BF16 tensor peak"
 DEFAULT_WORKLOAD = "causal_b2h32n8192d128"
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_PEAK_GBS = 6800.0
-KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_merge_kernel.cuh"]
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "attn_fwd_pair_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_merge_kernel.cuh"]
 
 
 def algorithmic_flops(B, H, Nq, Nk, d, causal, lens=None) -> float:

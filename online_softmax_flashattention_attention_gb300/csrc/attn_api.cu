@@ -15,6 +15,7 @@
 
 #include "../../include/attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_fwd_pair_kernel.cuh"
 #include "attn_merge_kernel.cuh"
 
 namespace {
@@ -236,38 +237,41 @@ struct Variant {
   bool soft = false;     // mixed exponentials (kDefaultSoftPairs) or ex2.approx only (default)
 };
 
-template <int D, bool kStates, int kSoft>
-attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
-                       int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
-                       uint32_t* status, const StateOut& so, const Variant& var, const Geometry& geo) {
-  using C = attn::FwdCfg<D>;
-  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft>;
-  static bool attr_set[kMaxDevices] = {};  // one flag per device for this instantiation
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!attr_set[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
-      if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      attr_set[dev] = true;
-    }
+// Sets max dynamic shared memory once per device for a kernel instantiation.
+template <typename Kernel>
+attn_status set_smem_attr(Kernel kernel, int bytes, int dev, bool* done) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    done[dev] = true;
   }
+  return ATTN_OK;
+}
+
+// Tensor maps of Q, K, V (and O unless the launch writes partial states) and the kernel
+// parameters every forward kernel shares.
+template <int D, bool kStates>
+attn_status make_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                        int Nk, float scale, int causal, const int32_t* lens, uint32_t* status, const StateOut& so,
+                        const Variant& var, const Geometry& geo, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
+                        CUtensorMap* mo, attn::FwdParams* pp) {
   const int BH = B * H;
-  CUtensorMap mq, mk, mv, mo;
   attn_status st;
-  if ((st = make_map(&mq, Q, D, geo.q_rows, H, geo.map_b, geo.qs)) != ATTN_OK) return st;
+  if ((st = make_map(mq, Q, D, geo.q_rows, H, geo.map_b, geo.qs)) != ATTN_OK) return st;
   if (kStates) {
-    mo = mq;  // never used: the partial-state epilogue stores with plain writes
-  } else if ((st = make_map(&mo, O, D, geo.q_rows, H, geo.map_b, geo.os)) != ATTN_OK) {
+    *mo = *mq;  // never used: the partial-state epilogue stores with plain writes
+  } else if ((st = make_map(mo, O, D, geo.q_rows, H, geo.map_b, geo.os)) != ATTN_OK) {
     return st;
   }
   if (geo.k_rows > 0) {
-    if ((st = make_map(&mk, K, D, geo.k_rows, H, geo.map_b, geo.ks)) != ATTN_OK) return st;
-    if ((st = make_map(&mv, V, D, geo.k_rows, H, geo.map_b, geo.vs)) != ATTN_OK) return st;
+    if ((st = make_map(mk, K, D, geo.k_rows, H, geo.map_b, geo.ks)) != ATTN_OK) return st;
+    if ((st = make_map(mv, V, D, geo.k_rows, H, geo.map_b, geo.vs)) != ATTN_OK) return st;
   } else {  // never read: every row is fully masked
-    mk = mq;
-    mv = mq;
+    *mk = *mq;
+    *mv = *mq;
   }
-  attn::FwdParams p;
+  attn::FwdParams& p = *pp;
   p.BH = BH;
   p.H = H;
   p.Nq = Nq;
@@ -295,16 +299,64 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   p.os_b = geo.cu_q ? 0 : geo.os[0];  // packed sequences address rows from cu_q, not by batch
   p.os_h = geo.os[1];
   p.os_r = geo.os[2];
-  const long long items = static_cast<long long>(p.num_qtiles) * BH * p.num_splits;
-  p.num_items = static_cast<int>(items);
+  p.num_items = static_cast<int>(static_cast<long long>(p.num_qtiles) * BH * p.num_splits);
+  return ATTN_OK;
+}
+
+template <int D, bool kStates, int kSoft>
+attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                       int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
+                       uint32_t* status, const StateOut& so, const Variant& var, const Geometry& geo) {
+  using C = attn::FwdCfg<D>;
+  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft>;
+  static bool attr_set[kMaxDevices] = {};  // one flag per device for this instantiation
+  attn_status st;
+  if ((st = set_smem_attr(kernel, C::kSmemAlloc, dev, attr_set)) != ATTN_OK) return st;
+  CUtensorMap mq, mk, mv, mo;
+  attn::FwdParams p;
+  if ((st = make_launch<D, kStates>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, status, so, var, geo, &mq,
+                                    &mk, &mv, &mo, &p)) != ATTN_OK)
+    return st;
   // persistent: one CTA per SM (shared and tensor memory allow no second), each walking
   // its items
   const int sms = sm_count(dev);
-  const unsigned grid = static_cast<unsigned>(std::min<long long>(items, sms > 0 ? sms : 1));
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
   kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
+}
+
+// d = 64, O and LSE out: two query tiles per CTA (attn_fwd_pair_kernel), when there are
+// enough pairs of tiles to give every SM one.
+template <int kSoft>
+attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
+                        int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
+                        uint32_t* status, const Variant& var, const Geometry& geo) {
+  using C = attn::PairCfg;
+  auto kernel = attn::attn_fwd_pair_kernel<kSoft>;
+  static bool attr_set[kMaxDevices] = {};
+  attn_status st;
+  if ((st = set_smem_attr(kernel, C::kSmemAlloc, dev, attr_set)) != ATTN_OK) return st;
+  CUtensorMap mq, mk, mv, mo;
+  attn::FwdParams p;
+  if ((st = make_launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, status, StateOut{}, var, geo,
+                                   &mq, &mk, &mv, &mo, &p)) != ATTN_OK)
+    return st;
+  p.num_items = static_cast<int>(static_cast<long long>((p.num_qtiles + 1) / 2) * p.BH);  // pairs of tiles
+  const int sms = sm_count(dev);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
+  kernel<<<grid, attn::kPairThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+// Whether a d = 64 forward takes the two-tile kernel: enough pairs of query tiles for
+// every SM to get one (fewer, and single tiles spread the work over more SMs).
+bool use_pair_kernel(int dev, int B, int H, const Geometry& geo) {
+  const long long pairs = static_cast<long long>(B) * H * (((geo.grid_q + attn::kBM - 1) / attn::kBM + 1) / 2);
+  return pairs >= sm_count(dev);
 }
 
 template <int D, bool kStates>
@@ -312,6 +364,14 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
                    float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
                    const StateOut& so = StateOut{}, const Variant& var = Variant{}, const Geometry* geo = nullptr) {
   const Geometry g = geo ? *geo : dense_geometry(B, H, Nq, Nk, D);
+  if constexpr (D == 64 && !kStates) {
+    if (use_pair_kernel(dev, B, H, g)) {
+      if (var.soft)
+        return launch_pair<kDefaultSoftPairs<64>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev,
+                                                  status, var, g);
+      return launch_pair<0>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, var, g);
+    }
+  }
   if (var.soft)
     return launch_one<D, kStates, kDefaultSoftPairs<D>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream,
                                                         dev, status, so, var, g);
