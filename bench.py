@@ -119,6 +119,16 @@ def algorithmic_bytes(B, H, Nq, Nk, d, lens=None, splits=0) -> float:
     return read + write
 
 
+def fused_kernel_name(B, H, Nq, d, sms):
+    """The kernel the library runs for a forward with O and LSE out: at d = 64, two query
+    tiles per CTA once there are at least as many pairs of tiles as SMs (attn_api.cu,
+    use_pair_kernel), else one tile per CTA."""
+    pairs = B * H * ((-(-Nq // 128) + 1) // 2)
+    if d == 64 and pairs >= sms:
+        return "attn_fwd_pair_kernel (d = 64, two query tiles per CTA)"
+    return f"attn_fwd_kernel<{d}>"
+
+
 def load_traffic(workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
     try:
@@ -621,7 +631,8 @@ def main():
     ridge = peak * 1e12 / (hbm_peak * 1e9)
     key = w["name"] + ("" if args.path == "fused" else ":splitkv") + ("" if args.layout == "bhsd" else ":" + args.layout)
     traffic = load_traffic(key)
-    kname = f"attn_fwd_kernel<{d}>" + ("" if args.path == "fused" else " (states)")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kname = fused_kernel_name(B, H, Nq, d, sms) if args.path == "fused" else f"attn_fwd_kernel<{d}> (states)"
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -717,7 +728,8 @@ def main_varlen(args, world, rank, local):
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
            "roofline": roofline_entry(flops / kbytes, peak * 1e12 / (hbm_peak * 1e9), tflops, peak, peak_src, kbytes,
                                       ms_kernel, hbm_peak, hbm_src, load_traffic(name), flops,
-                                      f"attn_fwd_kernel<{d}> (packed sequences)"),
+                                      fused_kernel_name(B, H, max(lengths), d, torch.cuda.get_device_properties(dev)
+                                                        .multi_processor_count) + " (packed sequences)"),
            "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": None}
     if rank == 0:
         print(json.dumps(out), flush=True)
