@@ -334,8 +334,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       float l = 0.f;        // running denominator
       // Checking a barrier costs a long round trip even when its phase completed long ago,
       // so the checks are issued early as non-blocking tests (as in attn_fwd_kernel): s_full
-      // of the tile's next product during this block's exponentials, pv_done of its previous
-      // product before their last chunk.  Only a "not yet" leads to the (bounded) wait.
+      // of the tile's next product and pv_done of its previous product, before the last
+      // chunk of this block's exponentials.  Only a "not yet" leads to the (bounded) wait.
       bool s_seen = false;
       for (int j = 0; j < it.nmax; ++j) {
         const int q = qbase + 2 * j + t;
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           constexpr bool kSoft = decltype(soft_tag)::value;
 #pragma unroll
           for (int x4 = 0; x4 < kBN / 32; ++x4) {
-            if (x4 == 0)
+            if (x4 == kBN / 32 - 1)
               s_seen = j + 1 < it.nmax && mbar_test_wait(bar_s_full(qx % kPairSBufs), (qx / kPairSBufs) & 1);
             if (x4 == 3)
               pv_seen = j > 0 && mbar_test_wait(bar_pv_done(qp % kPairSBufs), (qp / kPairSBufs) & 1);
