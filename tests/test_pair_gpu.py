@@ -176,3 +176,29 @@ def test_two_tile_kernel_withheld_block_times_out(monkeypatch):
     O2, L2 = run_cuda(x)
     O_ref, L_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], False, None)
     compare(O2, L2, O_ref, L_ref)
+
+
+def test_two_tile_kernel_random_shapes_bitwise():
+    """Seeded random shapes (tile counts 1..9, ragged Nq, Nk from 0, causal or not, padding
+    lengths from 0 to past Nk): the two-tile kernel on the whole problem equals the one-tile
+    kernel run a batch at a time, bit for bit."""
+    rng = np.random.default_rng(2024)
+    n_sm = sms()
+    for case in range(14):
+        nqt = int(rng.integers(1, 10))
+        per_head = (nqt + 1) // 2
+        H = max(1, (n_sm - 1) // per_head)            # one batch stays below the SM count
+        B = -(-n_sm // (H * per_head)) + int(rng.integers(0, 3))
+        Nq = int(rng.integers(max(1, 128 * (nqt - 1) + 1), 128 * nqt + 1))
+        Nk = int(rng.integers(0, 1500))
+        causal = bool(rng.integers(0, 2))
+        lens = None
+        if rng.integers(0, 2):
+            lens = [int(v) for v in rng.integers(0, Nk + 200, size=B)]
+            lens[int(rng.integers(0, B))] = 0
+        assert pairs(B, H, Nq) >= n_sm > pairs(1, H, Nq)
+        x = custom(B, H, Nq, Nk, causal, seed=1800 + case, lens=lens)
+        O2, L2 = run_cuda(x)
+        O1, L1 = _one_batch_at_a_time(x, causal, lens)
+        assert np.array_equal(O1, O2), (case, B, H, Nq, Nk, causal, lens)
+        assert np.array_equal(L1, L2), (case, B, H, Nq, Nk, causal, lens)
