@@ -18,11 +18,11 @@
 // or lies past the end of its sequence) still takes its place in the sequence with an
 // empty product, which moves the barriers on without any MMA or arithmetic, so that each
 // tile's products stay two apart and every wait stays within one phase of its barrier.
-// Product q writes its scores into score buffer q % 3.  With three buffers for two tiles a score product waits only for the P V
-// product three places before it, which belongs to the other tile or to this tile's block
-// two back, never to the block just before: neither tile runs S -> softmax -> P V -> S in
-// series, and while one tile's softmax warps work the tensor core runs the other tile's
-// products.  Tensor memory: three score buffers of 128 columns (P over the first 64 of
+// Product q writes its scores into score buffer q % 3.  With three buffers for two tiles a
+// score product waits only for the P V product three places before it, which is always
+// the other tile's, never this tile's previous one: neither tile runs S -> softmax ->
+// P V -> S in series, and while one tile's softmax warps work the tensor core runs the
+// other tile's products.  Tensor memory: three score buffers of 128 columns (P over the first 64 of
 // its own buffer) and o~ of each tile (64 columns each), 512 columns in all.
 #pragma once
 
