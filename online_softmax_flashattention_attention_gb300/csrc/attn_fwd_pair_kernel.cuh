@@ -232,7 +232,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
   } else if (warp == kPairWarpS || warp == kPairWarpPv) {
     // ================================================================ MMA issuers
-    if (lane == 0) {
+    // The whole warp runs the issuer loop (warp-uniform control flow; measured on GB300,
+    // 7-9 % faster than one lane running it alone); one elected lane issues each MMA and
+    // commit.
+    {
       // descriptor high word: stride 1024 B, version 1, 128-byte swizzle (as attn_fwd_kernel)
       const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
       int e = (warp == kPairWarpS) ? 0 : 1;  // this issuer's ring entries: K_j even, V_j odd
@@ -245,16 +248,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const PairItem it = decode_pair(p, item);
         if (it.nmax == 0) continue;
         if (warp == kPairWarpS) {
-          ok = mbar_wait(bar_q_full, kq & 1, wc, 3);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full, kq & 1, wc, 3));
           const uint32_t klo = (sRing >> 4) | (1u << 16);
           for (int j = 0; ok && j < it.nmax; ++j, e += 2) {
             const int slot = e % C::kSlots;
-            if (!(ok = mbar_wait(bar_full(slot), (e / C::kSlots) & 1, wc, 5))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_full(slot), (e / C::kSlots) & 1, wc, 5)))) break;
             for (int t = 0; t < 2; ++t) {
               const int q = qn + 2 * j + t;
               const int b = q % kPairSBufs;
               // buffer b last held the P of product q - 3: its P V product must have read it
-              if (q >= kPairSBufs && !(ok = mbar_wait(bar_pv_done(b), ((q - kPairSBufs) / kPairSBufs) & 1, wc, 4)))
+              if (q >= kPairSBufs && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_pv_done(b), ((q - kPairSBufs) / kPairSBufs) & 1, wc, 4))))
                 break;
               if (j < it.nblk[t]) {
                 tc_fence_after();
@@ -263,28 +266,28 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 const uint32_t blo = klo + slot * (C::kTileBytes >> 4);
 #pragma unroll
                 for (int ks = 0; ks < C::D / 16; ++ks)
-                  mma_ss(tmem + C::col_s(b), (static_cast<uint64_t>(dhi) << 32) | (qlo + ks * 2),
+                  mma_ss_elect(tmem + C::col_s(b), (static_cast<uint64_t>(dhi) << 32) | (qlo + ks * 2),
                          (static_cast<uint64_t>(dhi) << 32) | (blo + ks * 2), C::kIdescS, ks > 0 ? 1u : 0u);
               }
-              mma_commit(bar_s_full(b));  // an empty product commits no MMA of its own
+              mma_commit_elect(bar_s_full(b));  // an empty product commits no MMA of its own
             }
             if (!ok) break;
-            mma_commit(bar_free(slot));  // K_j has been read by both tiles' products
+            mma_commit_elect(bar_free(slot));  // K_j has been read by both tiles' products
           }
           if (!ok) break;
-          mma_commit(bar_q_free);
+          mma_commit_elect(bar_q_free);
           ++kq;
         } else {
           const uint32_t vlo = (sRing >> 4) | (static_cast<uint32_t>(C::kTileBytes >> 4) << 16);
           for (int j = 0; ok && j < it.nmax; ++j, e += 2) {
             const int slot = e % C::kSlots;
-            if (!(ok = mbar_wait(bar_full(slot), (e / C::kSlots) & 1, wc, 7))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_full(slot), (e / C::kSlots) & 1, wc, 7)))) break;
             for (int t = 0; t < 2; ++t) {
               const int q = qn + 2 * j + t;
               const int b = q % kPairSBufs;
-              if (!(ok = mbar_wait_poll(bar_p_full(b), (q / kPairSBufs) & 1, wc, 6))) break;
+              if (!(ok = __all_sync(0xffffffffu, mbar_wait_poll(bar_p_full(b), (q / kPairSBufs) & 1, wc, 6)))) break;
               if (j >= it.nblk[t]) {  // an empty product
-                mma_commit(bar_pv_done(b));
+                mma_commit_elect(bar_pv_done(b));
                 continue;
               }
               tc_fence_after();
@@ -294,21 +297,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               const uint32_t blo = vlo + slot * (C::kTileBytes >> 4);
 #pragma unroll
               for (int ks = 0; ks < kBN / 16; ++ks)
-                mma_ts(tmem + C::col_o(t), tmem + C::col_s(b) + ks * 8,
+                mma_ts_elect(tmem + C::col_o(t), tmem + C::col_s(b) + ks * 8,
                        (static_cast<uint64_t>(dhi) << 32) | (blo + ks * (16 * 128 >> 4)), C::kIdescO,
                        (j > 0 || ks > 0) ? 1u : 0u);
-              mma_commit(bar_pv_done(b));
-              if (j + 1 == it.nblk[t]) mma_commit(bar_o_done(t));  // o~_t is complete
+              mma_commit_elect(bar_pv_done(b));
+              if (j + 1 == it.nblk[t]) mma_commit_elect(bar_o_done(t));  // o~_t is complete
             }
             if (!ok) break;
-            mma_commit(bar_free(slot));  // V_j has been read by both tiles' products
+            mma_commit_elect(bar_free(slot));  // V_j has been read by both tiles' products
           }
         }
         qn += 2 * it.nmax;
       }
       // every MMA this thread issued must finish before tensor memory is released
       const int di = warp == kPairWarpS ? 0 : 1;
-      mma_commit(bar_drain(di));
+      mma_commit_elect(bar_drain(di));
       mbar_wait_drain(bar_drain(di), 0, p.timeout_ns);
     }
   } else {
