@@ -297,3 +297,20 @@ def test_parity_full_size_sampled(name):
         assert np.all(np.isfinite(LSE[1]))
     else:
         assert np.all(np.isfinite(LSE))
+
+
+# ------------------------------------------------------------------ very long sequences, sampled rows
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_parity_131072_keys_sampled(d):
+    """Causal B1 H4 N131072: 1024 query tiles per head and up to 1024 key blocks per tile,
+    many items per CTA (d = 64 takes the two-tile kernel); sampled rows against the oracle,
+    every row finite."""
+    B, H, N = 1, 4, 131072
+    x = custom(B, H, N, N, d, True, seed=4100 + d, qk=("normal", 0.0, 0.5))
+    O, LSE = run_cuda(x)
+    picks = sample_rows(B, H, N, n_random=8, seed=d)
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], True, None, picks)
+    idx = tuple(np.array(picks).T)
+    compare(O[idx], LSE[idx], O_ref, LSE_ref)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(LSE))
