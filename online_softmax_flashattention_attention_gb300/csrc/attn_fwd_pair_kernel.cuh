@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   if (warp == kPairWarpTma) {
     // ================================================================ producer
-    if (lane == 0) {
+    // Warp-wide like the MMA issuers below: one elected lane issues each copy.
+    {
       const uint64_t pol_kv = policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
       int e = 0;   // ring entries loaded so far over all pairs (K_j, then V_j): slot e % kSlots
@@ -201,25 +202,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const PairItem it = decode_pair(p, item);
         if (it.nmax == 0) continue;
         // the previous pair's Q tiles must have been read by its last S product
-        if (kq > 0 && !mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13)) break;
-        mbar_arrive_expect_tx(bar_q_full, ((it.nblk[0] > 0) + (it.nblk[1] > 0)) * C::kTileBytes);
+        if (kq > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13))) break;
+        mbar_arrive_expect_tx_elect(bar_q_full, ((it.nblk[0] > 0) + (it.nblk[1] > 0)) * C::kTileBytes);
         for (int t = 0; t < 2; ++t)
           if (it.nblk[t] > 0)
-            tma_load_4d(sQ + t * C::kTileBytes, &tmQ, bar_q_full, 0, it.q_base + it.q0[t], it.hh, it.bcoord, pol_q);
+            tma_load_4d_elect(sQ + t * C::kTileBytes, &tmQ, bar_q_full, 0, it.q_base + it.q0[t], it.hh, it.bcoord,
+                              pol_q);
         ++kq;
         for (int j = 0; ok && j < it.nmax; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++e) {
             const int slot = e % C::kSlots;
-            if (!mbar_wait(bar_free(slot), ((e / C::kSlots) & 1) ^ 1, wc, 1 + kv)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_free(slot), ((e / C::kSlots) & 1) ^ 1, wc, 1 + kv))) {
               ok = false;
               break;
             }
             last[slot] = -1;
             // the test hook withholds K of one block: its full barrier never completes
             if (kv == 1 || j != p.fault_block) {
-              mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
-              tma_load_4d(sRing + slot * C::kTileBytes, kv ? &tmV : &tmK, bar_full(slot), 0, it.k_base + j * kBN,
-                          it.hh, it.bcoord, pol_kv);
+              mbar_arrive_expect_tx_elect(bar_full(slot), C::kTileBytes);
+              tma_load_4d_elect(sRing + slot * C::kTileBytes, kv ? &tmV : &tmK, bar_full(slot), 0,
+                                it.k_base + j * kBN, it.hh, it.bcoord, pol_kv);
               last[slot] = e;
             }
           }
@@ -257,7 +259,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               const int q = qn + 2 * j + t;
               const int b = q % kPairSBufs;
               // buffer b last held the P of product q - 3: its P V product must have read it
-              if (q >= kPairSBufs && !(ok = __all_sync(0xffffffffu, mbar_wait(bar_pv_done(b), ((q - kPairSBufs) / kPairSBufs) & 1, wc, 4))))
+              if (q >= kPairSBufs &&
+                  !(ok = __all_sync(0xffffffffu,
+                                    mbar_wait(bar_pv_done(b), ((q - kPairSBufs) / kPairSBufs) & 1, wc, 4))))
                 break;
               if (j < it.nblk[t]) {
                 tc_fence_after();
