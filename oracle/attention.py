@@ -4,7 +4,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its
 ``cpu_baseline`` leg and ``--impl reference`` arm) may import this module.  The
 CUDA library never calls it and shares no code with it.
 
-Sources (web pages this build restates):
+Sources (web pages this module restates):
 
 * [OS] "2.2b: FlashAttention -- Online Softmax" (hf-cn0.pages.dev, blog of
   atharv6f): "The Softmax Formula", "The Numerical Stability Problem",
