@@ -352,11 +352,13 @@ attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, fl
   return ATTN_OK;
 }
 
-// Whether a d = 64 forward takes the two-tile kernel: enough pairs of query tiles for
-// every SM to get one (fewer, and single tiles spread the work over more SMs).
-bool use_pair_kernel(int dev, int B, int H, const Geometry& geo) {
+// Whether a d = 64 forward takes the two-tile kernel (measured on GB300): with a causal
+// mask, when every SM gets a pair of query tiles (with fewer, single tiles spread the
+// unequal causal tiles over more SMs); without one, as soon as the pairs fill more than
+// half the SMs (a single-tile grid would then need two rounds of equal tiles).
+bool use_pair_kernel(int dev, int B, int H, const Geometry& geo, int causal) {
   const long long pairs = static_cast<long long>(B) * H * (((geo.grid_q + attn::kBM - 1) / attn::kBM + 1) / 2);
-  return pairs >= sm_count(dev);
+  return causal ? pairs >= sm_count(dev) : 2 * pairs > sm_count(dev);
 }
 
 template <int D, bool kStates>
@@ -365,7 +367,7 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
                    const StateOut& so = StateOut{}, const Variant& var = Variant{}, const Geometry* geo = nullptr) {
   const Geometry g = geo ? *geo : dense_geometry(B, H, Nq, Nk, D);
   if constexpr (D == 64 && !kStates) {
-    if (use_pair_kernel(dev, B, H, g)) {
+    if (use_pair_kernel(dev, B, H, g, causal)) {
       if (var.soft)
         return launch_pair<kDefaultSoftPairs<64>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev,
                                                   status, var, g);

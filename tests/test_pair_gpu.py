@@ -1,8 +1,9 @@
 """The d = 64 forward with two query tiles per CTA, against the fp64 oracle.
 
-At d = 64 the library runs two adjacent query tiles per CTA once there are at least as
-many pairs of tiles as SMs; smaller problems keep one tile per CTA.  Every case here has
-more pairs than SMs, so it runs the two-tile kernel, with odd tile counts (a pair whose
+At d = 64 the library runs two adjacent query tiles per CTA once the pairs of tiles are
+at least as many as the SMs (causal) or more than half of them (no causal mask); smaller
+problems keep one tile per CTA.  Every case here is above that threshold, so it runs the
+two-tile kernel, with odd tile counts (a pair whose
 second tile lies past the end), tail rows, padded and fully masked batches, bottom-right
 causal masks with Nq > Nk (a pair whose first tile sees no key while the second does)
 and Nq < Nk, packed sequences, a strided layout, the options of attn_fwd_ex and the
@@ -39,6 +40,12 @@ def pairs(B, H, Nq):
     return B * H * ((-(-Nq // 128) + 1) // 2)
 
 
+def takes_pair_kernel(B, H, Nq, causal):
+    """The library's rule: causal, at least one pair per SM; otherwise more than half."""
+    n = pairs(B, H, Nq)
+    return n >= sms() if causal else 2 * n > sms()
+
+
 CASES = [
     # B, H, Nq, Nk, causal, lens
     (4, 40, 300, 300, True, None),                 # 3 tiles per head: the second pair has one tile
@@ -52,7 +59,7 @@ CASES = [
 
 @pytest.mark.parametrize("B,H,Nq,Nk,causal,lens", CASES)
 def test_two_tile_kernel_matches_oracle(B, H, Nq, Nk, causal, lens):
-    assert pairs(B, H, Nq) >= sms(), "the case must take the two-tile kernel"
+    assert takes_pair_kernel(B, H, Nq, causal), "the case must take the two-tile kernel"
     x = custom(B, H, Nq, Nk, causal, seed=1300 + B * H + Nq + Nk, lens=lens)
     O, LSE = run_cuda(x)
     O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"])
@@ -72,12 +79,12 @@ def _one_batch_at_a_time(x, causal, lens):
 
 @pytest.mark.parametrize("B,H,Nq,Nk,causal,lens", [
     (4, 40, 300, 300, True, None),
-    (4, 40, 512, 700, False, [700, 0, 129, 1]),
+    (4, 36, 512, 700, False, [700, 0, 129, 1]),
     (2, 72, 384, 256, True, None),
 ])
 def test_two_tile_kernel_equals_one_tile_kernel_bitwise(B, H, Nq, Nk, causal, lens):
     x = custom(B, H, Nq, Nk, causal, seed=1400 + Nq, lens=lens)
-    assert pairs(B, H, Nq) >= sms() > pairs(1, H, Nq)
+    assert takes_pair_kernel(B, H, Nq, causal) and not takes_pair_kernel(1, H, Nq, causal)
     O2, L2 = run_cuda(x)
     O1, L1 = _one_batch_at_a_time(x, causal, lens)
     assert np.array_equal(O1, O2)
@@ -93,7 +100,7 @@ def test_two_tile_kernel_packed_sequences():
     H, d, n = 4, 64, 90
     lq = rng.integers(0, 700, size=n)
     lk = lq + rng.integers(0, 100, size=n)
-    assert n * H * ((-(-int(lq.max()) // 128) + 1) // 2) >= sms()
+    assert takes_pair_kernel(n, H, int(lq.max()), True)
     total_q, total_k = int(lq.sum()), int(lk.sum())
     w = dict(name="packed", B=1, H=H, Nq=total_q, Nk=total_k, d=d, causal=False, qk=("normal", 0.0, 1.0),
              v=("normal", 0.0, 1.0), seed=33, lens=None, plant=None, scale=1.0 / math.sqrt(d))
@@ -187,16 +194,17 @@ def test_two_tile_kernel_random_shapes_bitwise():
     for case in range(14):
         nqt = int(rng.integers(1, 10))
         per_head = (nqt + 1) // 2
-        H = max(1, (n_sm - 1) // per_head)            # one batch stays below the SM count
+        causal = bool(rng.integers(0, 2))
+        # one batch stays below the two-tile threshold, the whole problem reaches the SM count
+        H = max(1, ((n_sm - 1) if causal else (n_sm // 2)) // per_head)
         B = -(-n_sm // (H * per_head)) + int(rng.integers(0, 3))
         Nq = int(rng.integers(max(1, 128 * (nqt - 1) + 1), 128 * nqt + 1))
         Nk = int(rng.integers(0, 1500))
-        causal = bool(rng.integers(0, 2))
         lens = None
         if rng.integers(0, 2):
             lens = [int(v) for v in rng.integers(0, Nk + 200, size=B)]
             lens[int(rng.integers(0, B))] = 0
-        assert pairs(B, H, Nq) >= n_sm > pairs(1, H, Nq)
+        assert takes_pair_kernel(B, H, Nq, causal) and not takes_pair_kernel(1, H, Nq, causal)
         x = custom(B, H, Nq, Nk, causal, seed=1800 + case, lens=lens)
         O2, L2 = run_cuda(x)
         O1, L1 = _one_batch_at_a_time(x, causal, lens)
