@@ -119,12 +119,13 @@ def algorithmic_bytes(B, H, Nq, Nk, d, lens=None, splits=0) -> float:
     return read + write
 
 
-def fused_kernel_name(B, H, Nq, d, sms):
+def fused_kernel_name(B, H, Nq, d, sms, causal=True):
     """The kernel the library runs for a forward with O and LSE out: at d = 64, two query
-    tiles per CTA once there are at least as many pairs of tiles as SMs (attn_api.cu,
-    use_pair_kernel), else one tile per CTA."""
+    tiles per CTA once the pairs of tiles are at least as many as the SMs (causal) or more
+    than half of them (no causal mask) (attn_api.cu, use_pair_kernel), else one tile per
+    CTA."""
     pairs = B * H * ((-(-Nq // 128) + 1) // 2)
-    if d == 64 and pairs >= sms:
+    if d == 64 and (pairs >= sms if causal else 2 * pairs > sms):
         return "attn_fwd_pair_kernel (d = 64, two query tiles per CTA)"
     return f"attn_fwd_kernel<{d}>"
 
@@ -632,7 +633,8 @@ def main():
     key = w["name"] + ("" if args.path == "fused" else ":splitkv") + ("" if args.layout == "bhsd" else ":" + args.layout)
     traffic = load_traffic(key)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    kname = fused_kernel_name(B, H, Nq, d, sms) if args.path == "fused" else f"attn_fwd_kernel<{d}> (states)"
+    kname = (fused_kernel_name(B, H, Nq, d, sms, causal) if args.path == "fused"
+             else f"attn_fwd_kernel<{d}> (states)")
     out = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -729,7 +731,7 @@ def main_varlen(args, world, rank, local):
            "roofline": roofline_entry(flops / kbytes, peak * 1e12 / (hbm_peak * 1e9), tflops, peak, peak_src, kbytes,
                                       ms_kernel, hbm_peak, hbm_src, load_traffic(name), flops,
                                       fused_kernel_name(B, H, max(lengths), d, torch.cuda.get_device_properties(dev)
-                                                        .multi_processor_count) + " (packed sequences)"),
+                                                        .multi_processor_count, causal) + " (packed sequences)"),
            "e2e": e2e, "gpu_launches": args.steps, "clocks": clocks, "cpu_baseline": None}
     if rank == 0:
         print(json.dumps(out), flush=True)
