@@ -226,14 +226,17 @@ def test_host_buffer_entry_point():
     assert np.array_equal(Oh.float().numpy(), O_dev) and np.array_equal(Lh.numpy(), LSE_dev)
 
 
-@pytest.mark.parametrize("B,H,N,causal,lens", [(1, 12, 8192, True, None), (2, 10, 4096, False, [4096, 1500])])
-def test_host_entry_point_pipelined_chunks(B, H, N, causal, lens):
+@pytest.mark.parametrize("B,H,N,causal,lens,d", [(1, 12, 8192, True, None, 128),
+                                                 (2, 10, 4096, False, [4096, 1500], 128),
+                                                 (1, 24, 8192, True, None, 64)])
+def test_host_entry_point_pipelined_chunks(B, H, N, causal, lens, d):
     """Inputs big enough for attn_fwd_host to cut the heads into several chunks (uneven
-    ones in the first case) whose copies overlap the forward: the result must equal the
-    device entry point bit for bit, and the oracle on sampled rows."""
+    ones in the first case; at d = 64 each chunk takes the two-tile kernel) whose copies
+    overlap the forward: the result must equal the device entry point bit for bit, and
+    the oracle on sampled rows."""
     import torch
     import online_softmax_flashattention_attention_gb300 as pkg
-    x = custom(B, H, N, N, 128, causal, seed=77 + B, lens=lens)
+    x = custom(B, H, N, N, d, causal, seed=77 + B + d, lens=lens)
     pin = lambda c: torch.from_numpy(np.ascontiguousarray(c).view(np.int16)).view(torch.bfloat16).pin_memory()  # noqa
     Qh, Kh, Vh = pin(x["Q"]), pin(x["K"]), pin(x["V"])
     Oh = torch.full_like(Qh, float("nan")).pin_memory()
