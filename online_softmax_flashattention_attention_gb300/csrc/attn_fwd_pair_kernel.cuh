@@ -12,7 +12,8 @@
 //   warps 4-7  softmax of tile 1 (the same lanes)
 //   warp 8     producer: TMA loads of the two Q tiles and of K_j, V_j into one ring of
 //              shared-memory slots (K_j and V_j take one slot each, in load order)
-//   warp 9     S issuer, warp 10 P V issuer (one thread each)
+//   warp 9     S issuer, warp 10 P V issuer (each warp runs its loop as a whole; one
+//              elected lane issues every MMA and commit)
 // The products of a pair of tiles form one sequence: for each key block j the pair loads,
 // tile 0's, then tile 1's, q = 2 j + t.  A tile that lacks block j (it sees fewer keys,
 // or lies past the end of its sequence) still takes its place in the sequence with an
