@@ -278,6 +278,8 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   p.Nk = Nk;
   p.num_qtiles = (geo.grid_q + attn::kBM - 1) / attn::kBM;
   p.causal = causal ? 1 : 0;
+  p.rank_major = 0;
+  p.order_div = p.num_qtiles;
   p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.lens = lens;
   p.lse = LSE;
@@ -303,6 +305,14 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   return ATTN_OK;
 }
 
+// Causal problems whose K and V take at most this much run every head's longest tiles
+// first (FwdParams::rank_major): with K/V of all heads in L2 at once, the order evens out
+// the CTAs' work; above it, heads in order keep each head's K/V in L2 while it runs.
+constexpr long long kRankMajorMaxKvBytes = 96ll << 20;
+
+// K and V of every head, bytes.
+long long kv_footprint(int B, int H, int Nk, int D) { return 4ll * B * H * Nk * D; }
+
 template <int D, bool kStates, int kSoft>
 attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                        int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
@@ -317,6 +327,8 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   if ((st = make_launch<D, kStates>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, status, so, var, geo, &mq,
                                     &mk, &mv, &mo, &p)) != ATTN_OK)
     return st;
+  if (!kStates && causal && !geo.cu_q && kv_footprint(B, H, Nk, D) <= kRankMajorMaxKvBytes) p.rank_major = 1;
+  p.order_div = p.rank_major ? p.BH : p.num_qtiles;
   // persistent: one CTA per SM (shared and tensor memory allow no second), each walking
   // its items
   const int sms = sm_count(dev);
@@ -344,6 +356,8 @@ attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, fl
                                    &mq, &mk, &mv, &mo, &p)) != ATTN_OK)
     return st;
   p.num_items = static_cast<int>(static_cast<long long>((p.num_qtiles + 1) / 2) * p.BH);  // pairs of tiles
+  if (causal && !geo.cu_q && kv_footprint(B, H, Nk, 64) <= kRankMajorMaxKvBytes) p.rank_major = 1;
+  p.order_div = p.rank_major ? p.BH : (p.num_qtiles + 1) / 2;
   const int sms = sm_count(dev);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
   kernel<<<grid, attn::kPairThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);

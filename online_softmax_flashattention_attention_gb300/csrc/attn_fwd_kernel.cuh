@@ -58,6 +58,8 @@ struct FwdParams {
   int BH, H, Nq, Nk;
   int num_qtiles;          // ceil(Nq / 128)
   int causal;
+  int rank_major;          // item order: 1 = tile rank major, 0 = head major (see decode)
+  int order_div;           // B H when rank major, else the tiles (two-tile kernel: pairs) per head
   float c;                 // scale * log2(e)
   const int32_t* lens;     // per-batch key lengths or null
   float* lse;              // [BH, Nq]
@@ -171,10 +173,14 @@ __device__ __forceinline__ Item decode(const FwdParams& p, int item) {
   const int nqt = p.num_qtiles;
   it.split = item % p.num_splits;
   const int unit = item / p.num_splits;
-  // heads in order (their K/V stay in L2 while their tiles run); within a head, causal
-  // tiles longest first
-  it.bh = unit / nqt;
-  int qtile = unit - it.bh * nqt;
+  // Head major: heads in order (their K/V stay in L2 while their tiles run).  Rank major:
+  // tile rank r of every head, then rank r + 1; the host picks it for causal problems
+  // whose K/V all fit in L2, where the snake of item_of over every head's longest tiles
+  // first evens out the CTAs' work.  Either way a head's causal tiles go longest first.
+  const int ua = unit / p.order_div;
+  const int ub = unit - ua * p.order_div;
+  it.bh = p.rank_major ? ub : ua;
+  int qtile = p.rank_major ? ua : ub;
   if (p.causal) qtile = nqt - 1 - qtile;
   it.b = it.bh / p.H;
   it.hh = it.bh - it.b * p.H;

@@ -76,10 +76,12 @@ struct PairItem {
 __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item) {
   PairItem it;
   const int npairs = (p.num_qtiles + 1) >> 1;
-  // heads in order (their K/V stay in L2 while their pairs run); within a head, causal
-  // pairs longest first
-  it.bh = item / npairs;
-  int pair = item - it.bh * npairs;
+  // as decode: head major (heads in order) or rank major (pair rank r of every head, then
+  // r + 1), order_div = npairs or B H; within a head, causal pairs longest first
+  const int ua = item / p.order_div;
+  const int ub = item - ua * p.order_div;
+  it.bh = p.rank_major ? ub : ua;
+  int pair = p.rank_major ? ua : ub;
   if (p.causal) pair = npairs - 1 - pair;
   it.b = it.bh / p.H;
   it.hh = it.bh - it.b * p.H;
