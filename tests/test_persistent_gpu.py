@@ -96,3 +96,23 @@ def test_many_packed_sequences():
             O_ref[h], L_ref[h] = oracle.attention_head(oracle.bf16_to_f64(Qp[rq, h]), oracle.bf16_to_f64(Kp[rk, h]),
                                                        oracle.bf16_to_f64(Vp[rk, h]), x["scale"], True)
         compare(Of[rq].transpose(1, 0, 2), Lf[:, rq], O_ref, L_ref)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_rank_major_order_leaves_results_unchanged(d):
+    """Causal problems whose K and V fit in L2 run every head's longest tiles first (the
+    rank-major item order).  A tile's arithmetic does not depend on which CTA runs it or
+    when, so the whole problem must equal, bit for bit, its heads run one per call, where
+    the order is trivially head major.  (At d = 64 the whole problem takes the two-tile
+    kernel and a single head the one-tile kernel; the two agree bit for bit there.)"""
+    B, H, N = 2, 40, 700
+    lens = [700, 333]
+    assert 4 * B * H * N * d <= 96 << 20, "the case must take the rank-major order"
+    x = custom(B, H, N, N, d, True, seed=2100 + d, lens=lens)
+    O, L = run_cuda(x)
+    for b in range(B):
+        for h in range(H):
+            xs = dict(x, **{k: np.ascontiguousarray(x[k][b:b + 1, h:h + 1]) for k in ("Q", "K", "V")})
+            Oh, Lh = run_cuda(xs, lens=[lens[b]])
+            assert np.array_equal(Oh[0, 0], O[b, h]), (b, h)
+            assert np.array_equal(Lh[0, 0], L[b, h]), (b, h)
