@@ -647,6 +647,12 @@ def main():
            "cpu_baseline": cpu,
            "cpu_blocked": cpu_blocked,
            "variants": variants}
+    if lens is not None:  # key padding: `value` counts the valid keys; the nominal count beside it
+        nominal = algorithmic_flops(B, H, Nq, Nk, d, causal)
+        out["nominal"] = {"value": value * nominal / flops if flops > 0 else None, "unit": "TFLOP/s",
+                          "flops_per_step": nominal, "flops_per_step_valid_keys": flops,
+                          "note": "4 B H Nq Nk d (halved when causal): every key counted as if unpadded; "
+                                  "the line's value counts only the keys the padding leaves visible"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg:
