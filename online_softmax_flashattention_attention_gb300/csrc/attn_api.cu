@@ -12,6 +12,7 @@
 #include <cstring>
 #include <algorithm>
 #include <mutex>
+#include <utility>
 
 #include "../../include/attn.h"
 #include "attn_fwd_kernel.cuh"
@@ -305,6 +306,27 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   return ATTN_OK;
 }
 
+// Launches `kernel` with programmatic stream serialization: it may be scheduled on the SMs
+// the previous kernel in `stream` has already left, run its prologue there (barriers,
+// tensor-memory allocation, descriptor prefetch) and wait in griddep_wait() for that
+// kernel to finish before it touches global memory.  Stream order is kept for everything
+// the kernels read and write.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Causal problems whose K and V take at most this much run every head's longest tiles
 // first (FwdParams::rank_major): with K/V of all heads in L2 at once, the order evens out
 // the CTAs' work; above it, heads in order keep each head's K/V in L2 while it runs.
@@ -333,8 +355,7 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   // its items
   const int sms = sm_count(dev);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
-  kernel<<<grid, attn::kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mo, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kernel, grid, attn::kThreads, C::kSmemAlloc, stream, mq, mk, mv, mo, p);
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }
@@ -360,8 +381,7 @@ attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, fl
   p.order_div = p.rank_major ? p.BH : (p.num_qtiles + 1) / 2;
   const int sms = sm_count(dev);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
-  kernel<<<grid, attn::kPairThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kernel, grid, attn::kPairThreads, C::kSmemAlloc, stream, mq, mk, mv, p);
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }
@@ -743,11 +763,8 @@ attn_status launch_merge(const float* o_st, const float* m_st, const float* l_st
   constexpr long long kRowsPerBlock = attn::kMergeThreads / 32;
   const long long want = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   const unsigned grid = static_cast<unsigned>(std::min<long long>(want, static_cast<long long>(sms) * 8));
-  if (d == 128)
-    attn::attn_merge_kernel<128><<<grid, attn::kMergeThreads, 0, stream>>>(mp);
-  else
-    attn::attn_merge_kernel<64><<<grid, attn::kMergeThreads, 0, stream>>>(mp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = d == 128 ? launch_pdl(attn::attn_merge_kernel<128>, grid, attn::kMergeThreads, 0, stream, mp)
+                           : launch_pdl(attn::attn_merge_kernel<64>, grid, attn::kMergeThreads, 0, stream, mp);
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "merge launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }

@@ -300,6 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above touched only shared and tensor memory and the kernel parameters; a
+  // launch that overlaps the previous kernel's tail waits here for it to finish.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kWarpTma) {
     // ================================================================ producer

@@ -187,6 +187,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // as in attn_fwd_kernel: the previous kernel has finished from here on
+  griddep_launch_dependents();
 
   if (warp == kPairWarpTma) {
     // ================================================================ producer

@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const MergePa
   constexpr int kChunk = 8;       // states loaded together: one round of independent loads
   constexpr float kLog2e = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
+  griddep_wait();  // the states kernel before it in the stream has finished
+  griddep_launch_dependents();
   const long long warps = static_cast<long long>(gridDim.x) * (kMergeThreads / 32);
   for (long long row = static_cast<long long>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
        row < p.rows; row += warps) {

@@ -11,6 +11,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may be scheduled before the previous kernel in its stream has finished.
+// griddep_wait() blocks until every prerequisite grid has completed and its memory
+// operations are visible (without that launch attribute it returns at once), so a kernel
+// calls it before its first global-memory access; griddep_launch_dependents() lets the
+// next such kernel be scheduled once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
