@@ -296,6 +296,7 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   p.st_l = so.l;
   p.cu_q = geo.cu_q;
   p.cu_k = geo.cu_k;
+  p.seq_sort = (geo.cu_q && B > 1 && B <= attn::kMaxSortedSeqs) ? 1 : 0;
   p.total_q = static_cast<int>(geo.q_rows);
   p.total_k = static_cast<int>(geo.k_rows);
   p.o = static_cast<__nv_bfloat16*>(O);
@@ -355,7 +356,9 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
   // its items
   const int sms = sm_count(dev);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
-  cudaError_t e = launch_pdl(kernel, grid, attn::kThreads, C::kSmemAlloc, stream, mq, mk, mv, mo, p);
+  // only packed-sequence launches use the sequence order's shared memory
+  const int smem = p.seq_sort ? C::kSmemAlloc : C::kSmemAllocNoPerm;
+  cudaError_t e = launch_pdl(kernel, grid, attn::kThreads, smem, stream, mq, mk, mv, mo, p);
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }
@@ -381,7 +384,8 @@ attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, fl
   p.order_div = p.rank_major ? p.BH : (p.num_qtiles + 1) / 2;
   const int sms = sm_count(dev);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(p.num_items, sms > 0 ? sms : 1));
-  cudaError_t e = launch_pdl(kernel, grid, attn::kPairThreads, C::kSmemAlloc, stream, mq, mk, mv, p);
+  const int smem = p.seq_sort ? C::kSmemAlloc : C::kSmemAllocNoPerm;
+  cudaError_t e = launch_pdl(kernel, grid, attn::kPairThreads, smem, stream, mq, mk, mv, p);
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "kernel launch: %s", cudaGetErrorString(e));
   return ATTN_OK;
 }

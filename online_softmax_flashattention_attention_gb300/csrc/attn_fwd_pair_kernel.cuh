@@ -48,8 +48,10 @@ struct PairCfg {
   // o_done[2], drain[2]
   static constexpr int kNumBars = 2 + 2 * kSlots + 3 * kPairSBufs + 4;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tensor-memory base, abort flag
-  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kOffPerm = kOffMisc + 16;           // uint16 order of packed sequences
+  static constexpr int kSmemBytes = kOffPerm + 2 * kMaxSortedSeqs;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack to align the base to 1024 B
+  static constexpr int kSmemAllocNoPerm = kOffPerm + 1024; // launches without seq_sort
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
   __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * b; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 128u * kPairSBufs + 64u * t; }
@@ -73,7 +75,7 @@ struct PairItem {
   bool valid[2];           // the tile has rows in its sequence
 };
 
-__device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item) {
+__device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item, const uint16_t* seq_perm) {
   PairItem it;
   const int npairs = (p.num_qtiles + 1) >> 1;
   // as decode: head major (heads in order) or rank major (pair rank r of every head, then
@@ -91,6 +93,10 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item) {
   it.Nk = p.Nk;
   it.bcoord = it.b;
   if (p.cu_q) {
+    if (p.seq_sort) {  // as in decode: the sequence of this rank in decreasing work
+      it.b = seq_perm[it.b];
+      it.bh = it.b * p.H + it.hh;
+    }
     const int qs = min(max(__ldg(p.cu_q + it.b), 0), p.total_q);
     const int qe = min(max(__ldg(p.cu_q + it.b + 1), qs), p.total_q);
     const int ks = min(max(__ldg(p.cu_k + it.b), 0), p.total_k);
@@ -189,6 +195,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // as in attn_fwd_kernel: the previous kernel has finished from here on
   griddep_launch_dependents();
+  uint16_t* seq_perm = reinterpret_cast<uint16_t*>(smem + C::kOffPerm);
+  if (p.seq_sort) rank_sequences(p, p.BH / p.H, reinterpret_cast<float*>(smem + C::kOffQ), seq_perm);
 
   if (warp == kPairWarpTma) {
     // ================================================================ producer
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
         if (item >= p.num_items) break;
-        const PairItem it = decode_pair(p, item);
+        const PairItem it = decode_pair(p, item, seq_perm);
         if (it.nmax == 0) continue;
         // the previous pair's Q tiles must have been read by its last S product
         if (kq > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13))) break;
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
         if (item >= p.num_items) break;
-        const PairItem it = decode_pair(p, item);
+        const PairItem it = decode_pair(p, item, seq_perm);
         if (it.nmax == 0) continue;
         if (warp == kPairWarpS) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full, kq & 1, wc, 3));
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const int item = item_of(ri, cta, G);
       if (item >= p.num_items) break;
-      const PairItem it = decode_pair(p, item);
+      const PairItem it = decode_pair(p, item, seq_perm);
       const int qbase = qn;
       qn += 2 * it.nmax;
       const int row = it.q0[t] + r;
