@@ -63,15 +63,19 @@ def test_many_items_split_states():
     compare(O.float().cpu().numpy().astype(np.float64), LSE.cpu().numpy().astype(np.float64), O_ref, LSE_ref)
 
 
-def test_many_packed_sequences():
-    """Packed sequences: 70 of them, 3 heads, lengths 0..400: several items per CTA, many
-    of them past the end of their (shorter) sequence."""
+@pytest.mark.parametrize("n,max_len,H,d,seed", [
+    (70, 400, 3, 128, 5),    # ranked by work in shared memory (at most 512 sequences)
+    (600, 120, 2, 64, 6),    # more than 512: the order of cu_seqlens
+])
+def test_many_packed_sequences(n, max_len, H, d, seed):
+    """Packed sequences of lengths 0..max_len: several items per CTA, many of them past the
+    end of their (shorter) sequence; up to 512 sequences the kernel walks them in
+    decreasing work, beyond that in the order given."""
     import torch
     import online_softmax_flashattention_attention_gb300 as pkg
-    rng = np.random.default_rng(5)
-    H, d = 3, 128
-    lq = rng.integers(0, 400, size=70)
-    lk = lq + rng.integers(0, 200, size=70)
+    rng = np.random.default_rng(seed)
+    lq = rng.integers(0, max_len, size=n)
+    lk = lq + rng.integers(0, max_len // 2, size=n)
     total_q, total_k = int(lq.sum()), int(lk.sum())
     w = dict(name="packed", B=1, H=H, Nq=total_q, Nk=total_k, d=d, causal=False, qk=("normal", 0.0, 1.0),
              v=("normal", 0.0, 1.0), seed=31, lens=None, plant=None, scale=1.0 / math.sqrt(d))
@@ -86,7 +90,7 @@ def test_many_packed_sequences():
     pkg.status_sync()
     Of = O.float().cpu().numpy().astype(np.float64)
     Lf = LSE.cpu().numpy().astype(np.float64)
-    for b in range(70):
+    for b in range(n):
         if lq[b] == 0:
             continue
         rq, rk = slice(cu_q[b], cu_q[b + 1]), slice(cu_k[b], cu_k[b + 1])
