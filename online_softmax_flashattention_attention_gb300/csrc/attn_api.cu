@@ -296,7 +296,7 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   p.st_l = so.l;
   p.cu_q = geo.cu_q;
   p.cu_k = geo.cu_k;
-  p.seq_sort = (geo.cu_q && B > 1 && B <= attn::kMaxSortedSeqs) ? 1 : 0;
+  p.seq_sort = (geo.cu_q && B > 1 && B <= attn::kMaxSortedSeqs) ? 1 : 0;  // read by the packed kernels only
   p.total_q = static_cast<int>(geo.q_rows);
   p.total_k = static_cast<int>(geo.k_rows);
   p.o = static_cast<__nv_bfloat16*>(O);
@@ -336,12 +336,12 @@ constexpr long long kRankMajorMaxKvBytes = 96ll << 20;
 // K and V of every head, bytes.
 long long kv_footprint(int B, int H, int Nk, int D) { return 4ll * B * H * Nk * D; }
 
-template <int D, bool kStates, int kSoft>
+template <int D, bool kStates, int kSoft, bool kPacked>
 attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                        int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
                        uint32_t* status, const StateOut& so, const Variant& var, const Geometry& geo) {
   using C = attn::FwdCfg<D>;
-  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft>;
+  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft, kPacked>;
   static bool attr_set[kMaxDevices] = {};  // one flag per device for this instantiation
   attn_status st;
   if ((st = set_smem_attr(kernel, C::kSmemAlloc, dev, attr_set)) != ATTN_OK) return st;
@@ -365,12 +365,12 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
 
 // d = 64, O and LSE out: two query tiles per CTA (attn_fwd_pair_kernel), when there are
 // enough pairs of tiles to give every SM one.
-template <int kSoft>
+template <int kSoft, bool kPacked>
 attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                         int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
                         uint32_t* status, const Variant& var, const Geometry& geo) {
   using C = attn::PairCfg;
-  auto kernel = attn::attn_fwd_pair_kernel<kSoft>;
+  auto kernel = attn::attn_fwd_pair_kernel<kSoft, kPacked>;
   static bool attr_set[kMaxDevices] = {};
   attn_status st;
   if ((st = set_smem_attr(kernel, C::kSmemAlloc, dev, attr_set)) != ATTN_OK) return st;
@@ -399,24 +399,39 @@ bool use_pair_kernel(int dev, int B, int H, const Geometry& geo, int causal) {
   return causal ? pairs >= sm_count(dev) : 2 * pairs > sm_count(dev);
 }
 
+// kPacked: packed sequences (geo.cu_q set), the kernels' instantiation that may rank them.
+template <int D, bool kStates, bool kPacked>
+attn_status launch_as(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
+                      float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
+                      const StateOut& so, const Variant& var, const Geometry& g) {
+  if constexpr (D == 64 && !kStates) {
+    if (use_pair_kernel(dev, B, H, g, causal)) {
+      if (var.soft)
+        return launch_pair<kDefaultSoftPairs<64>, kPacked>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens,
+                                                           stream, dev, status, var, g);
+      return launch_pair<0, kPacked>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, var,
+                                     g);
+    }
+  }
+  if (var.soft)
+    return launch_one<D, kStates, kDefaultSoftPairs<D>, kPacked>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens,
+                                                                 stream, dev, status, so, var, g);
+  return launch_one<D, kStates, 0, kPacked>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status,
+                                            so, var, g);
+}
+
 template <int D, bool kStates>
 attn_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
                    float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
                    const StateOut& so = StateOut{}, const Variant& var = Variant{}, const Geometry* geo = nullptr) {
   const Geometry g = geo ? *geo : dense_geometry(B, H, Nq, Nk, D);
-  if constexpr (D == 64 && !kStates) {
-    if (use_pair_kernel(dev, B, H, g, causal)) {
-      if (var.soft)
-        return launch_pair<kDefaultSoftPairs<64>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev,
-                                                  status, var, g);
-      return launch_pair<0>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, var, g);
-    }
+  if constexpr (!kStates) {
+    if (g.cu_q)
+      return launch_as<D, false, true>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, so,
+                                       var, g);
   }
-  if (var.soft)
-    return launch_one<D, kStates, kDefaultSoftPairs<D>>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream,
-                                                        dev, status, so, var, g);
-  return launch_one<D, kStates, 0>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, so, var,
-                                   g);
+  return launch_as<D, kStates, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, stream, dev, status, so,
+                                      var, g);
 }
 
 // Options -> kernel variant; NULL means the defaults.

@@ -205,6 +205,9 @@ __device__ __noinline__ void rank_sequences(const FwdParams& p, int B, float* sc
   __syncthreads();
 }
 
+// kPacked: a launch over packed sequences (cu_q set), which may take them in the order of
+// seq_perm; the other launches' code has no such step.
+template <bool kPacked>
 __device__ __forceinline__ Item decode(const FwdParams& p, int item, const uint16_t* seq_perm) {
   Item it;
   const int nqt = p.num_qtiles;
@@ -229,9 +232,11 @@ __device__ __forceinline__ Item decode(const FwdParams& p, int item, const uint1
   it.bcoord = it.b;
   it.valid = true;
   if (p.cu_q) {
-    if (p.seq_sort) {  // the unit's sequence is the one of its rank in decreasing work
-      it.b = seq_perm[it.b];
-      it.bh = it.b * p.H + it.hh;
+    if constexpr (kPacked) {
+      if (p.seq_sort) {  // the unit's sequence is the one of its rank in decreasing work
+        it.b = seq_perm[it.b];
+        it.bh = it.b * p.H + it.hh;
+      }
     }
     const int qs = min(max(__ldg(p.cu_q + it.b), 0), p.total_q);
     const int qe = min(max(__ldg(p.cu_q + it.b + 1), qs), p.total_q);
@@ -277,7 +282,7 @@ __device__ __forceinline__ int item_of(int r, int c, int G) { return r * G + ((r
 // P V product has finished, and leaves by one TMA store; the softmax warps then hand that
 // stage back to the producer (v_free) instead of the P V issuer.  At d = 128 each thread
 // stores its row of O straight from registers.
-template <int D, bool kStates, int kSoftPairs>
+template <int D, bool kStates, int kSoftPairs, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -346,7 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
   uint16_t* seq_perm = reinterpret_cast<uint16_t*>(smem + C::kOffPerm);
-  if (p.seq_sort) rank_sequences(p, p.BH / p.H, reinterpret_cast<float*>(smem + C::kOffQ), seq_perm);
+  if constexpr (kPacked) {
+    if (p.seq_sort) rank_sequences(p, p.BH / p.H, reinterpret_cast<float*>(smem + C::kOffQ), seq_perm);
+  }
 
   if (warp == kWarpTma) {
     // ================================================================ producer
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
         if (item >= p.num_items) break;
-        const Item it = decode(p, item, seq_perm);
+        const Item it = decode<kPacked>(p, item, seq_perm);
         if (it.nblk == 0) continue;
         // the previous tile's Q must have been read by its last S product
         if (kq > 0 && !mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13)) break;
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ri = 0; ok; ++ri) {
           const int item = item_of(ri, cta, G);
           if (item >= p.num_items) break;
-          const Item it = decode(p, item, seq_perm);
+          const Item it = decode<kPacked>(p, item, seq_perm);
           if (it.nblk == 0) continue;
           ok = mbar_wait(bar_q_full, kq & 1, wc, 3);
           for (int j = 0; ok && j < it.nblk; ++j, ++g) {
@@ -450,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ri = 0; ok; ++ri) {
           const int item = item_of(ri, cta, G);
           if (item >= p.num_items) break;
-          const Item it = decode(p, item, seq_perm);
+          const Item it = decode<kPacked>(p, item, seq_perm);
           if (it.nblk == 0) continue;
           // The first product of a tile overwrites o~.  The softmax warps read the previous
           // tile's o~ out before they write this tile's first P, and P_0 is awaited below,
@@ -493,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const int item = item_of(ri, cta, G);
       if (item >= p.num_items) break;
-      const Item it = decode(p, item, seq_perm);
+      const Item it = decode<kPacked>(p, item, seq_perm);
       if (!it.valid) continue;  // a tile past the end of a shorter packed sequence
       const int row = it.q0 + r;
       const int limit = row_key_limit(row, it.kv_len, it.Nq, it.Nk, p.causal);

@@ -75,6 +75,7 @@ struct PairItem {
   bool valid[2];           // the tile has rows in its sequence
 };
 
+template <bool kPacked>  // as in decode
 __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item, const uint16_t* seq_perm) {
   PairItem it;
   const int npairs = (p.num_qtiles + 1) >> 1;
@@ -93,9 +94,11 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item, co
   it.Nk = p.Nk;
   it.bcoord = it.b;
   if (p.cu_q) {
-    if (p.seq_sort) {  // as in decode: the sequence of this rank in decreasing work
-      it.b = seq_perm[it.b];
-      it.bh = it.b * p.H + it.hh;
+    if constexpr (kPacked) {
+      if (p.seq_sort) {  // as in decode: the sequence of this rank in decreasing work
+        it.b = seq_perm[it.b];
+        it.bh = it.b * p.H + it.hh;
+      }
     }
     const int qs = min(max(__ldg(p.cu_q + it.b), 0), p.total_q);
     const int qe = min(max(__ldg(p.cu_q + it.b + 1), qs), p.total_q);
@@ -135,7 +138,7 @@ __device__ __forceinline__ PairItem decode_pair(const FwdParams& p, int item, co
 // completed (a tile's previous product is two places back, and tcgen05 commits of one
 // thread complete in order), and the phase after it needs an arrival that comes after the
 // wait.
-template <int kSoftPairs>
+template <int kSoftPairs, bool kPacked>
 __global__ void __launch_bounds__(kPairThreads, 1)
     attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -196,7 +199,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   griddep_wait();  // as in attn_fwd_kernel: the previous kernel has finished from here on
   griddep_launch_dependents();
   uint16_t* seq_perm = reinterpret_cast<uint16_t*>(smem + C::kOffPerm);
-  if (p.seq_sort) rank_sequences(p, p.BH / p.H, reinterpret_cast<float*>(smem + C::kOffQ), seq_perm);
+  if constexpr (kPacked) {
+    if (p.seq_sort) rank_sequences(p, p.BH / p.H, reinterpret_cast<float*>(smem + C::kOffQ), seq_perm);
+  }
 
   if (warp == kPairWarpTma) {
     // ================================================================ producer
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
         if (item >= p.num_items) break;
-        const PairItem it = decode_pair(p, item, seq_perm);
+        const PairItem it = decode_pair<kPacked>(p, item, seq_perm);
         if (it.nmax == 0) continue;
         // the previous pair's Q tiles must have been read by its last S product
         if (kq > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13))) break;
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
         if (item >= p.num_items) break;
-        const PairItem it = decode_pair(p, item, seq_perm);
+        const PairItem it = decode_pair<kPacked>(p, item, seq_perm);
         if (it.nmax == 0) continue;
         if (warp == kPairWarpS) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar_q_full, kq & 1, wc, 3));
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const int item = item_of(ri, cta, G);
       if (item >= p.num_items) break;
-      const PairItem it = decode_pair(p, item, seq_perm);
+      const PairItem it = decode_pair<kPacked>(p, item, seq_perm);
       const int qbase = qn;
       qn += 2 * it.nmax;
       const int row = it.q0[t] + r;
