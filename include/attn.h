@@ -31,6 +31,10 @@
  *
  * Ownership: the caller owns every buffer.  attn_fwd allocates no device memory per
  * call; the library keeps one small device status word per device, created on first use.
+ * Streams: every kernel is launched with programmatic stream serialization, so it may be
+ * scheduled while the previous kernel in the stream finishes; it touches no global
+ * memory before that kernel has completed and its writes are visible, so stream order
+ * holds for every buffer as with a plain launch.
  * Errors: every entry point returns an attn_status; no C++ exception crosses this ABI.
  * attn_last_error() gives a message for the calling thread's last failure.
  */
