@@ -303,6 +303,10 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   p.os_b = geo.cu_q ? 0 : geo.os[0];  // packed sequences address rows from cu_q, not by batch
   p.os_h = geo.os[1];
   p.os_r = geo.os[2];
+  // O's base and every row stride (bf16 elements) on 32 bytes: each row can be stored 32
+  // bytes at a time
+  p.o_v8 = ((reinterpret_cast<uintptr_t>(O) & 31) == 0 && (p.os_b * 2) % 32 == 0 && (p.os_h * 2) % 32 == 0 &&
+            (p.os_r * 2) % 32 == 0) ? 1 : 0;
   p.num_items = static_cast<int>(static_cast<long long>(p.num_qtiles) * BH * p.num_splits);
   return ATTN_OK;
 }
