@@ -5,4 +5,4 @@ reference legs; the CUDA library never uses it.
 """
 from .attention import (NEG_INF, attention, attention_head, attention_rows, attention_state_head,  # noqa: F401
                         attention_states, bf16_to_f64, finish_state, merge_states, online_softmax_attention,
-                        softmax_naive, softmax_safe, softmax_stats, visible, visible_row)
+                        softmax_naive, softmax_safe, softmax_stats, visible, visible_row, visible_rows)

@@ -160,28 +160,61 @@ def attention(Q, K, V, scale: float, causal: bool = False, lens=None):
     return O, LSE
 
 
-def attention_rows(Q, K, V, scale: float, causal: bool, lens, picks):
+def visible_rows(rows, Nq: int, Nk: int, causal: bool, key_len=None) -> np.ndarray:
+    """Rows ``rows`` of ``visible``: boolean [len(rows), Nk]."""
+    L = Nk if key_len is None else int(min(max(int(key_len), 0), Nk))
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    j = np.arange(Nk)[None, :]
+    vis = np.broadcast_to(j < L, (i.shape[0], Nk))
+    if causal:
+        vis = vis & (j <= i + (Nk - Nq))
+    return vis
+
+
+def attention_rows(Q, K, V, scale: float, causal: bool, lens, picks, chunk: int = 1024):
     """Oracle for selected rows only: picks is a list of (b, h, i).
 
-    Each row is computed on its own from its query vector, so this serves
-    problems too large to run whole on the CPU.  Returns (O [n, dv], LSE [n]).
+    Every row follows the three-pass definition of ``attention_head`` on its own
+    query vector ([FM] "Safe softmax"): s_j = scale * q . k_j with masked keys at
+    -inf, m = max s, l = sum exp(s_j - m), O = sum exp(s_j - m) v_j / l,
+    LSE = m + ln l; a row with no visible key has O = 0, LSE = -inf.  Rows never
+    interact, so the rows of one head are evaluated together, ``chunk`` at a time,
+    with that head's keys widened to float64 once; keys past the last key any row
+    of the chunk may see are masked for all of them and are left out (they would
+    only add exp(-inf) = 0 terms).  This serves problems too large to run whole on
+    the CPU.  Returns (O [n, dv], LSE [n]) in the order of ``picks``.
     """
     Nq, Nk = Q.shape[2], K.shape[2]
     dv = V.shape[3]
     O = np.zeros((len(picks), dv))
     LSE = np.full(len(picks), NEG_INF)
+    groups = {}
     for r, (b, h, i) in enumerate(picks):
-        q = _as_f64(Q[b, h, i:i + 1])
+        groups.setdefault((int(b), int(h)), []).append((r, int(i)))
+    for (b, h), members in groups.items():
         k = _as_f64(K[b, h])
         v = _as_f64(V[b, h])
         L = None if lens is None else int(lens[b])
-        s = scale * (k @ q[0])
-        s = np.where(visible_row(i, Nq, Nk, causal, L), s, NEG_INF)
-        m, l = softmax_stats(s)
-        if l > 0.0:
-            p = np.exp(s - m)
-            O[r] = (p @ v) / l
-            LSE[r] = m + np.log(l)
+        for c0 in range(0, len(members), chunk):
+            part = members[c0:c0 + chunk]
+            out = np.array([r for r, _ in part], dtype=np.int64)
+            rows = np.array([i for _, i in part], dtype=np.int64)
+            vis = visible_rows(rows, Nq, Nk, causal, L)
+            seen = np.nonzero(vis.any(axis=0))[0]
+            kmax = int(seen[-1]) + 1 if seen.size else 0
+            if kmax == 0:
+                continue                                    # every row fully masked
+            q = _as_f64(Q[b, h][rows])
+            s = scale * (q @ k[:kmax].T)
+            s = np.where(vis[:, :kmax], s, NEG_INF)
+            m = s.max(axis=1)                               # pass 1
+            live = m > NEG_INF
+            ref = np.where(live, m, 0.0)
+            p = np.exp(s - ref[:, None])                    # exp(-inf) = 0 for masked keys
+            l = p.sum(axis=1)                               # pass 2
+            acc = p @ v[:kmax]                              # pass 3
+            O[out[live]] = acc[live] / l[live, None]
+            LSE[out[live]] = m[live] + np.log(l[live])
     return O, LSE
 
 

@@ -247,6 +247,32 @@ def test_attention_rows_matches_attention():
     assert np.allclose(LSEr[fin], LSE.reshape(-1)[fin], rtol=1e-12)
 
 
+def test_attention_rows_any_order_and_chunking_against_brute_force():
+    """Rows picked out of order, repeated, over several heads and cut into chunks of three
+    must each equal the brute-force definition, in the order they were asked for."""
+    rng = np.random.default_rng(5)
+    B, H, Nq, Nk, d = 2, 3, 10, 13, 4
+    Q, K, V = (rng.normal(size=(B, H, n, d)) for n in (Nq, Nk, Nk))
+    lens = np.array([9, 0])
+    picks = [(1, 2, 3), (0, 1, 9), (0, 1, 0), (0, 0, 5), (0, 1, 9), (1, 0, 9), (0, 2, 4), (0, 1, 7), (0, 1, 2)]
+    for causal in (False, True):
+        Or, LSEr = oracle.attention_rows(Q, K, V, 0.5, causal, lens, picks, chunk=3)
+        for r, (b, h, i) in enumerate(picks):
+            Ob, LSEb = brute_force(Q[b, h], K[b, h], V[b, h], 0.5, causal, int(lens[b]))
+            assert np.allclose(Or[r], Ob[i], rtol=1e-12, atol=1e-14), (causal, r)
+            if np.isfinite(LSEb[i]):
+                assert abs(LSEr[r] - LSEb[i]) < 1e-12
+            else:
+                assert np.isneginf(LSEr[r]) and np.all(Or[r] == 0)
+
+
+def test_visible_rows_are_rows_of_visible():
+    for causal, L in ((False, None), (True, None), (True, 5), (False, 0)):
+        full = np.broadcast_to(oracle.visible(7, 9, causal, L), (7, 9))  # [1, Nk] without a causal mask
+        rows = [6, 0, 3, 3]
+        assert np.array_equal(oracle.visible_rows(rows, 7, 9, causal, L), full[rows])
+
+
 def test_bf16_decode():
     # 0x3F80 = 1.0, 0xC000 = -2.0, 0x7F80 = +inf, 0x0001 = smallest subnormal 2^-133
     got = oracle.bf16_to_f64(np.array([0x3F80, 0xC000, 0x7F80, 0x0001, 0x4049], dtype=np.uint16))
@@ -433,3 +459,46 @@ def test_mutation_mask_after_max_is_caught():
     bad, _, _ = oracle.online_softmax_attention(s, v, 4, valid=valid, _mutation="mask_after_max")
     assert abs(good - want) < 1e-12
     assert not abs(bad - want) < 1e-6
+
+
+def _threshold_recurrence(s, v, block, tau):
+    """The block-wise update with a reference that moves only when a block max passes it
+    by more than tau (the library's lazy-rescale option); returns the largest p, l and
+    |o~| met on the way and the final (o, l)."""
+    m, l, o = -np.inf, 0.0, np.zeros(v.shape[1])
+    pmax = lmax = omax = 0.0
+    for lo in range(0, len(s), block):
+        sb, vb = s[lo:lo + block], v[lo:lo + block]
+        mb = sb.max()
+        m_new = mb if mb > m + tau else m
+        alpha = np.exp(m - m_new) if m > -np.inf else 0.0
+        p = np.exp(sb - m_new)
+        l = alpha * l + p.sum()
+        o = alpha * o + p @ vb
+        m = m_new
+        pmax, lmax, omax = max(pmax, p.max()), max(lmax, l), max(omax, np.abs(o).max())
+    return pmax, lmax, omax, o / l, l
+
+
+@pytest.mark.parametrize("tau", [0.0, 5.5, 20.0])
+def test_lazy_rescale_stability_bound(tau):
+    """The bound stated for the lazy-rescale option ("FlashAttention math", "Proof of
+    numerical stability", restated for a reference that trails the max by up to tau):
+    p <= e^tau, l <= Nk e^tau, |o~| <= Nk e^tau max|V|; and the result is the softmax."""
+    rng = np.random.default_rng(int(tau * 10) + 1)
+    Nk, block = 1024, 128
+    v = rng.uniform(-100.0, 100.0, size=(Nk, 8))
+    cases = [rng.normal(scale=3.0, size=Nk),
+             (tau - 1e-9) * (np.arange(Nk) // block) + 0.0,          # rises by just under tau per block
+             (tau + 0.5) * (np.arange(Nk) // block) + rng.normal(scale=0.1, size=Nk)]
+    bound = math.exp(tau)
+    for s in cases:
+        pmax, lmax, omax, out, _ = _threshold_recurrence(s, v, block, tau)
+        assert pmax <= bound * (1 + 1e-12)
+        assert lmax <= Nk * bound * (1 + 1e-12)
+        assert omax <= Nk * bound * np.abs(v).max() * (1 + 1e-12)
+        O, _ = oracle.attention_head(np.array([[1.0]]), s[:, None], v, 1.0)
+        assert np.allclose(out, O[0], rtol=1e-10, atol=1e-9)
+    # the case that rises by just under tau reaches the bound within a factor e^-1e-9
+    pmax, *_ = _threshold_recurrence(cases[1], v, block, tau)
+    assert pmax >= bound * math.exp(-1e-6)
