@@ -275,29 +275,65 @@ def test_repeated_calls_deterministic():
     assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
 
 
-# ------------------------------------------------------------------ full-size workloads, sampled rows
+# ------------------------------------------------------------------ full-size workloads: every work item
 
 FULL = ["causal_b4h16n2048d128", "causal_b2h32n8192d128", "padded_planted_b2h8n4096d128",
         "causal_b1h32n32768d128", "causal_b1h32n32768d64"]
 
 
+def item_picks(B, H, Nq, seed):
+    """Two rows of every work item (b, h, 128-row query tile): a random row of the tile and
+    its last row (the longest one of a causal tile, the ragged end of the last tile)."""
+    rng = np.random.default_rng(seed)
+    picks = []
+    for b in range(B):
+        for h in range(H):
+            for t0 in range(0, Nq, 128):
+                t1 = min(Nq, t0 + 128)
+                picks += [(b, h, int(rng.integers(t0, t1))), (b, h, t1 - 1)]
+    return sorted(set(picks))
+
+
+def parity_report(name, part, err):
+    print(f"PARITY {name} {part}: max|dO|={err['max_abs_o']:.3e} mean|dO|={err['mean_abs_o']:.3e} "
+          f"max|dLSE|={err['max_abs_lse']:.3e} worst_ratio={err['worst_ratio']:.3f}")
+
+
 @pytest.mark.parametrize("name", FULL)
-def test_parity_full_size_sampled(name):
+def test_parity_full_size_every_item(name):
+    """Full-size workloads against the oracle: two rows of every (b, h, q-tile) work item,
+    so a scheduler or decode slip (wrong head, batch, causal offset or key range for any
+    item) is caught, plus one whole head row by row.  On the adversarial workload the rows
+    whose planted maximum sits in the first key tile (even rows) and in the last valid tile
+    (odd rows) are compared and reported separately."""
     x = gen.make_inputs(name)
     O, LSE = run_cuda(x)
     B, H, Nq = x["B"], x["H"], x["Nq"]
-    picks = sample_rows(B, H, Nq, n_random=40, seed=hash(name) % 1000)
-    if x["lens"] is not None:  # include rows of the fully masked batch and of the padded one
-        picks += [(0, 3, 10), (0, H - 1, Nq - 1), (1, 2, 2), (1, 5, 3)]
+    s_v = 100.0 if x["name"].startswith("padded") else 1.0
+    picks = item_picks(B, H, Nq, seed=sum(map(ord, name)))
     O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], x["causal"], x["lens"], picks)
     idx = tuple(np.array(picks).T)
-    s_v = 100.0 if x["name"].startswith("padded") else 1.0
-    compare(O[idx], LSE[idx], O_ref, LSE_ref, s_v=s_v)
+    parity_report(name, f"items ({len(picks)} rows)", compare(O[idx], LSE[idx], O_ref, LSE_ref, s_v=s_v))
+    # one whole head, every row (the padded workload: a head of the batch with keys)
+    hb = B - 1
+    hh = H // 2
+    whole = [(hb, hh, i) for i in range(Nq)]
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], x["causal"], x["lens"], whole)
+    err = compare(O[hb, hh], LSE[hb, hh], O_ref, LSE_ref, s_v=s_v)
+    parity_report(name, f"head (b={hb}, h={hh}), all {Nq} rows", err)
+    if "planted_key" in x:  # max in the first key tile (even rows) vs the last valid one (odd rows)
+        for part, sel in (("max in first tile (even rows)", slice(0, None, 2)),
+                          ("max in last valid tile (odd rows)", slice(1, None, 2))):
+            e = compare(O[hb, hh, sel], LSE[hb, hh, sel], O_ref[sel], LSE_ref[sel], s_v=s_v)
+            parity_report(name, f"head (b={hb}, h={hh}), {part}", e)
     # properties that hold everywhere: finite, fully masked batch exact
     assert np.all(np.isfinite(O))
     if x["lens"] is not None:
-        assert np.all(O[0] == 0) and np.all(np.isneginf(LSE[0]))
-        assert np.all(np.isfinite(LSE[1]))
+        dead = [b for b in range(B) if min(max(int(x["lens"][b]), 0), x["Nk"]) == 0]
+        for b in dead:
+            assert np.all(O[b] == 0) and np.all(np.isneginf(LSE[b]))
+        for b in set(range(B)) - set(dead):
+            assert np.all(np.isfinite(LSE[b]))
     else:
         assert np.all(np.isfinite(LSE))
 
