@@ -73,9 +73,10 @@ typedef enum {
  * once; a device-side wait timeout is reported by attn_status_sync.
  * Environment, read at every launch (all entry points):
  *   ATTN_WAIT_LIMIT_MS          limit of each device-side wait in ms (default 2000).
- *   ATTN_TEST_WITHHOLD_K_BLOCK  test hook only: the loader skips key block j (0-based) of
- *                               every tile, so the waits on it run out; the call then
- *                               reports ATTN_ERR_TIMEOUT and O / LSE are not written.
+ *   ATTN_TEST_WITHHOLD_K_BLOCK  test hook, honoured only while ATTN_ENABLE_TEST_HOOKS=1 is
+ *                               also set: the loader skips key block j (0-based) of every
+ *                               tile, so the waits on it run out; the call then reports
+ *                               ATTN_ERR_TIMEOUT and O / LSE are not written.
  */
 attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                      int Nk, int d, float scale, int causal, const int32_t* key_padding_lens, void* stream);
@@ -93,10 +94,18 @@ enum {
 typedef struct attn_options {
   size_t size;
   /* Lazy rescale: the running max m is moved (and l, o~ rescaled) only when a block's max
-   * exceeds it by more than this many natural-log units; in between, p = exp(s - m) may
-   * reach exp(threshold).  0 = the pages' rule (rescale whenever the max rises).  The
-   * result is the same in exact arithmetic: softmax is invariant to the reference
-   * ("FlashAttention math", "Safe softmax": any constant m).  Range [0, 20]. */
+   * exceeds it by more than tau = this many natural-log units.  0 = the pages' rule
+   * (rescale whenever the max rises).  The result is the same in exact arithmetic:
+   * softmax is invariant to the reference ("FlashAttention math", "Safe softmax": any
+   * constant m).  Range [0, 20].
+   * Stability bound ("FlashAttention math", "Proof of numerical stability", restated for
+   * a reference that may trail the max by up to tau): every score the recurrence meets
+   * is at most m + tau, so every probability p = exp(s - m) <= e^tau (<= 4.9e8 at
+   * * tau = 20, well inside the range of bf16 P and of fp32), the running sum
+   * l <= Nk * e^tau and |o~| <= Nk * e^tau * max|V| (per column).  The result is finite
+   * whenever Nk * e^tau * max|V| < FLT_MAX = 3.4e38 (at tau = 0 this is the plain fp32
+   * accumulation bound Nk * max|V|); inputs beyond it may overflow o~ to inf and are
+   * excluded.  Example: at tau = 20 and Nk = 2^20 keys, |V| must stay below 6.7e23. */
   float rescale_threshold;
   int exp2_mode;           /* ATTN_EXP2_* */
 } attn_options;
@@ -163,8 +172,10 @@ attn_status attn_fwd_host(const void* Q, const void* K, const void* V, void* O, 
 /* Free the attn_fwd_host workspace of the current device. */
 attn_status attn_release_workspace(void);
 
-/* Synchronise `stream`, then read and clear the device status word of the current
- * device: ATTN_ERR_TIMEOUT if a kernel's bounded wait ran out since the last check. */
+/* Synchronise `stream`, then read and clear the device status words of the current
+ * device (the one the allocating entry points use and, once attn_fwd_noalloc has run
+ * on the device, its fixed one): ATTN_ERR_TIMEOUT if a kernel's bounded wait ran out
+ * since the last check.  Reads and clears with plain copies; allocates nothing. */
 attn_status attn_status_sync(void* stream);
 
 /* Message for the calling thread's last non-OK status ("" if none). */
@@ -191,15 +202,20 @@ int attn_version(void);
  * ATTN_ERR_BAD_SHAPE (the forward kernel needs 4 bytes, so today no call is).
  *
  *  - The first call on a device does one-time set-up with that device current: it
- *    looks up the array's device address (cudaGetSymbolAddress) and sets the kernel
- *    attributes.  Make that first call before any stream capture.
- *  - Every call shares the array and it keeps the last call's contents: each call
- *    clears the status word on `stream` before its launch.  Calls that overlap on the
- *    GPU (different streams, or several host threads) race on that word, so their
- *    timeout reports can be lost or misattributed; serialise them if you rely on it.
+ *    looks up the array's device address (cudaGetSymbolAddress), sets the shared-memory
+ *    attribute of every kernel this entry point can launch (d = 128, d = 64 with one
+ *    and with two query tiles per CTA) and caches the SM count.  Make that first call
+ *    before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents.  Its status
+ *    word is the OR of every bounded wait that ran out since the word was last read; it
+ *    starts at zero and is cleared where it is read: by a call with check_status != 0
+ *    and by attn_status_sync.  Calls that overlap on the GPU (different streams, or
+ *    several host threads) share that word, so a timeout is reported to whichever of
+ *    them reads it first; serialise them if you rely on the attribution.
  *  - check_status == 0: asynchronous, like attn_fwd; a device-side wait that runs out
- *    still ends the kernel, but is not reported.  check_status != 0: the call
- *    synchronises `stream` and returns ATTN_ERR_TIMEOUT if a wait ran out.
+ *    still ends the kernel, and attn_status_sync (on a stream ordered after the call)
+ *    reports it later.  check_status != 0: the call synchronises `stream` and returns
+ *    ATTN_ERR_TIMEOUT if a wait ran out since the word was last read.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 attn_status attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,

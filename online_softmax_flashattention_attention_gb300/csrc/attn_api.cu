@@ -11,6 +11,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <utility>
 
@@ -36,6 +37,9 @@ attn_status fail(attn_status st, const char* fmt, ...) {
 
 std::mutex g_mu;
 uint32_t* g_status[kMaxDevices] = {};
+// Device address of the allocation-free entry point's status word, per device (null until
+// that entry point's first call on the device).
+uint32_t* g_noalloc_addr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -78,15 +82,16 @@ attn_status setup(int dev, uint32_t** status) {
   return ATTN_OK;
 }
 
-// SM count of a device, cached.
+// SM count of a device, cached (several host threads may fill the same slot: they
+// write the same value).
+std::atomic<int> g_sm_cache[kMaxDevices];
 int sm_count(int dev) {
-  static int cached[kMaxDevices] = {};
-  if (!cached[dev]) {
-    int n = 0;
+  int n = g_sm_cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-    cached[dev] = n;
+    g_sm_cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 // attn_fwd_host's copy streams and events, one set per device, created on first use.
@@ -184,7 +189,11 @@ unsigned long long wait_limit_ns() {
 
 // Test hook: ATTN_TEST_WITHHOLD_K_BLOCK=j makes every CTA's producer skip the load of key
 // block j, so the waits on it run out and the failure path can be exercised without a fault.
+// It is honoured only while ATTN_ENABLE_TEST_HOOKS=1 is set as well, so that a stray
+// variable in a user's environment cannot silently drop keys.
 int fault_block() {
+  const char* on = std::getenv("ATTN_ENABLE_TEST_HOOKS");
+  if (!on || std::strcmp(on, "1") != 0) return -1;
   const char* v = std::getenv("ATTN_TEST_WITHHOLD_K_BLOCK");
   if (v && *v) return static_cast<int>(std::strtol(v, nullptr, 10));
   return -1;
@@ -340,15 +349,27 @@ constexpr long long kRankMajorMaxKvBytes = 96ll << 20;
 // K and V of every head, bytes.
 long long kv_footprint(int B, int H, int Nk, int D) { return 4ll * B * H * Nk * D; }
 
+// The shared-memory attribute of one instantiation of each forward kernel, set once per
+// device (one flag per device and instantiation).
+template <int D, bool kStates, int kSoft, bool kPacked>
+attn_status fwd_kernel_attr(int dev) {
+  static bool attr_set[kMaxDevices] = {};
+  return set_smem_attr(attn::attn_fwd_kernel<D, kStates, kSoft, kPacked>, attn::FwdCfg<D>::kSmemAlloc, dev, attr_set);
+}
+template <int kSoft, bool kPacked>
+attn_status pair_kernel_attr(int dev) {
+  static bool attr_set[kMaxDevices] = {};
+  return set_smem_attr(attn::attn_fwd_pair_kernel<kSoft, kPacked>, attn::PairCfg::kSmemAlloc, dev, attr_set);
+}
+
 template <int D, bool kStates, int kSoft, bool kPacked>
 attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                        int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
                        uint32_t* status, const StateOut& so, const Variant& var, const Geometry& geo) {
   using C = attn::FwdCfg<D>;
   auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft, kPacked>;
-  static bool attr_set[kMaxDevices] = {};  // one flag per device for this instantiation
   attn_status st;
-  if ((st = set_smem_attr(kernel, C::kSmemAlloc, dev, attr_set)) != ATTN_OK) return st;
+  if ((st = fwd_kernel_attr<D, kStates, kSoft, kPacked>(dev)) != ATTN_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   attn::FwdParams p;
   if ((st = make_launch<D, kStates>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, status, so, var, geo, &mq,
@@ -375,9 +396,8 @@ attn_status launch_pair(const void* Q, const void* K, const void* V, void* O, fl
                         uint32_t* status, const Variant& var, const Geometry& geo) {
   using C = attn::PairCfg;
   auto kernel = attn::attn_fwd_pair_kernel<kSoft, kPacked>;
-  static bool attr_set[kMaxDevices] = {};
   attn_status st;
-  if ((st = set_smem_attr(kernel, C::kSmemAlloc, dev, attr_set)) != ATTN_OK) return st;
+  if ((st = pair_kernel_attr<kSoft, kPacked>(dev)) != ATTN_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   attn::FwdParams p;
   if ((st = make_launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, status, StateOut{}, var, geo,
@@ -673,15 +693,22 @@ attn_status attn_status_sync(void* stream) {
   int dev;
   attn_status st = get_device(&dev);
   if (st != ATTN_OK) return st;
-  uint32_t* status = g_status[dev];
-  if (!status) return ATTN_OK;
-  uint32_t v = 0;
-  if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return fail(ATTN_ERR_LAUNCH, "status read failed");
-  if (v) {
-    cudaMemset(status, 0, sizeof(uint32_t));
-    return fail(ATTN_ERR_TIMEOUT, "a bounded device wait ran out (status word 0x%x)", v);
+  // the status word of the allocating entry points, then the no-alloc entry point's one
+  uint32_t* words[2] = {g_status[dev], g_noalloc_addr[dev]};
+  uint32_t seen = 0;
+  for (uint32_t* w : words) {
+    if (!w) continue;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return fail(ATTN_ERR_LAUNCH, "status read failed");
+    if (v) {  // cleared in `stream` order, so a later launch's report is not wiped
+      cudaStream_t s = static_cast<cudaStream_t>(stream);
+      if (cudaMemsetAsync(w, 0, sizeof(uint32_t), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return fail(ATTN_ERR_LAUNCH, "status clear failed");
+      seen |= v;
+    }
   }
+  if (seen) return fail(ATTN_ERR_TIMEOUT, "a bounded device wait ran out (status word 0x%x)", seen);
   return ATTN_OK;
 }
 
@@ -702,27 +729,40 @@ constexpr int kNoAllocScratchWords = 64;
 constexpr size_t kNoAllocScratchBytes = kNoAllocScratchWords * sizeof(uint32_t);  // 256 B per device
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
 
-uint32_t* g_noalloc_addr[kMaxDevices] = {};
-
 // One-time set-up per device (that device current): kernel-facing address of the array,
-// device check and the tensor-map encoder.  No allocation.
+// device check, the tensor-map encoder, and every kernel attribute and cached value a later
+// call could otherwise set on first use (the shared-memory size of each forward kernel
+// this entry point can launch, the SM count).  No allocation.
 attn_status noalloc_setup(int dev, uint32_t** addr) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-      return fail(ATTN_ERR_NO_DEVICE, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  if (!g_noalloc_addr[dev]) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(ATTN_ERR_NO_DEVICE, "cuTensorMapEncodeTiled unavailable: %s", cudaGetErrorString(e));
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (g_noalloc_addr[dev]) {
+      *addr = g_noalloc_addr[dev];
+      return ATTN_OK;
+    }
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
       return fail(ATTN_ERR_NO_DEVICE, "cudaGetDeviceProperties failed");
     if (prop.major != 10 || prop.minor != 3)
       return fail(ATTN_ERR_NO_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, prop.major,
                   prop.minor);
+  }
+  // set_smem_attr takes the lock itself
+  attn_status st;
+  if ((st = fwd_kernel_attr<128, false, 0, false>(dev)) != ATTN_OK) return st;
+  if ((st = fwd_kernel_attr<64, false, 0, false>(dev)) != ATTN_OK) return st;
+  if ((st = pair_kernel_attr<0, false>(dev)) != ATTN_OK) return st;
+  sm_count(dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_noalloc_addr[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p)
@@ -751,14 +791,19 @@ extern "C" attn_status attn_fwd_noalloc(const void* Q, const void* K, const void
   uint32_t* scratch = nullptr;
   if ((st = noalloc_setup(dev, &scratch)) != ATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(scratch, 0, need, s);  // the array keeps the previous call's word
-  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "clearing the status word: %s", cudaGetErrorString(e));
+  // The status word is an OR of every bounded wait that ran out since it was last read:
+  // it starts at zero (the array is zero when the library's module loads) and is cleared
+  // only where it is read, here with check_status or by attn_status_sync.
   st = (d == 128) ? launch<128, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch)
                   : launch<64, false>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, key_padding_lens, s, dev, scratch);
   if (st != ATTN_OK || !check_status) return st;
   uint32_t word = 0;
-  e = cudaStreamSynchronize(s);
+  cudaError_t e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word) {
+    e = cudaMemsetAsync(scratch, 0, need, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "reading the status word: %s", cudaGetErrorString(e));
   if (word) return fail(ATTN_ERR_TIMEOUT, "a bounded device wait ran out (status word 0x%x)", word);
   return ATTN_OK;

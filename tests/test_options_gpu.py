@@ -152,3 +152,22 @@ def test_planted_workload_lazy_sampled_rows():
     O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], False, x["lens"], picks)
     idx = tuple(np.array(picks).T)
     compare(O[idx], LSE[idx], O_ref, LSE_ref, s_v=100.0)
+
+
+def test_largest_threshold_with_values_of_100():
+    """tau = 20, the largest threshold allowed, with the max rising by 19.5 (just under tau)
+    every other block, so that p reaches e^19.5 ~ 2.9e8 before the reference moves, and V
+    uniform in [-100, 100]: |o~| reaches ~4e12, far inside the stated bound
+    Nk e^tau max|V| < FLT_MAX, and the result must meet the s_V = 100 tolerance."""
+    import torch
+    Qt, Kt, _, q, k, _ = rising_max_problem(step=19.5)
+    rng = np.random.default_rng(21)
+    Vt = torch.from_numpy(rng.uniform(-100.0, 100.0, size=(1, 1, Kt.shape[2], Kt.shape[3])).astype(np.float32)
+                          ).to(torch.bfloat16).cuda()
+    v = Vt.float().cpu().numpy().astype(np.float64)
+    x = dict(scale=1.0, causal=False, lens=None)
+    for mode in (1, 2):
+        O, LSE = run_ex(x, 20.0, mode, Q=Qt, K=Kt, V=Vt)
+        assert np.all(np.isfinite(O)) and np.all(np.isfinite(LSE))
+        O_ref, LSE_ref = oracle.attention(q, k, v, 1.0, False, None)
+        compare(O, LSE, O_ref, LSE_ref, s_v=100.0)

@@ -172,6 +172,7 @@ def test_two_tile_kernel_withheld_block_times_out(monkeypatch):
     O = torch.empty_like(Q)
     LSE = torch.empty((B, H, N), device="cuda")
     monkeypatch.setenv("ATTN_WAIT_LIMIT_MS", "100")
+    monkeypatch.setenv("ATTN_ENABLE_TEST_HOOKS", "1")
     monkeypatch.setenv("ATTN_TEST_WITHHOLD_K_BLOCK", "1")
     pkg.attn_fwd(Q, K, V, O, LSE, scale=x["scale"])
     with pytest.raises(pkg.AttnError) as err:

@@ -3,20 +3,29 @@
 that must not grow its host's footprint).  Its scratch is a fixed array inside the
 library instead of cudaMalloc'd memory.
 
-Called through the C ABI with ctypes and compared with attn_fwd, under the parity
-tolerance of the other GPU tests, on two calls in a row (the second call reuses the
-array the first one left behind).  This file is collected last on purpose.
+Called through the C ABI with ctypes on two problems in a row (the second call reuses
+the array the first one left behind); each result is compared with the fp64 oracle
+under the parity tolerance of the other GPU tests, and with attn_fwd on the same inputs.
+A second test runs the entry point alone in a fresh process and checks that its first
+call takes no device memory.  This file is collected last on purpose.
 """
 import ctypes
+import json
 import math
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
 
 import gen
+import oracle
 from gpu_helpers import compare, run_cuda, to_device
 
 pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _lib():
@@ -54,14 +63,16 @@ def _run_noalloc(lib, x):
     return O.float().cpu().numpy().astype(np.float64), LSE.cpu().numpy().astype(np.float64)
 
 
-def test_noalloc_matches_attn_fwd_on_two_calls_in_a_row():
+def test_noalloc_matches_oracle_and_attn_fwd_on_two_calls_in_a_row():
     lib = _lib()
     problems = [_problem(2, 3, 300, 300, 128, True, seed=41, lens=[300, 170]),
                 _problem(1, 2, 256, 383, 64, False, seed=42)]
     for x in problems:
-        O_ref, LSE_ref = run_cuda(x)          # the existing entry point
-        O, LSE = _run_noalloc(lib, x)         # the allocation-free one
+        O, LSE = _run_noalloc(lib, x)          # the allocation-free entry point
+        O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], x["causal"], x["lens"])
         compare(O, LSE, O_ref, LSE_ref)
+        O_fwd, LSE_fwd = run_cuda(x)            # the existing entry point, same tolerance
+        compare(O, LSE, O_fwd, LSE_fwd)
 
 
 def test_noalloc_rejects_bad_arguments_like_attn_fwd():
@@ -69,3 +80,47 @@ def test_noalloc_rejects_bad_arguments_like_attn_fwd():
     rc = lib.attn_fwd_noalloc(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 1, 16, 16, 96, 0.1, 0, None, 1,
                               None)
     assert rc == -3
+
+
+_FRESH_PROCESS = r"""
+import ctypes, json, sys
+sys.path.insert(0, sys.argv[1])
+import torch
+import online_softmax_flashattention_attention_gb300 as pkg
+lib = pkg.load_library()
+f = lib.attn_fwd_noalloc
+vp, i = ctypes.c_void_p, ctypes.c_int
+f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp, i, vp]
+f.restype = i
+out = {}
+for d in (128, 64):  # d = 64 with many heads takes the two-tile kernel
+    H = 2 if d == 128 else 304
+    g = torch.Generator(device="cuda").manual_seed(d)
+    Q, K, V = (torch.randn(1, H, 384, d, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
+    O = torch.empty_like(Q)
+    L = torch.empty(1, H, 384, device="cuda")
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    rc = f(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(), 1, H, 384, 384, d, d ** -0.5, 1,
+           None, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    out[d] = dict(rc=rc, free_before=free0, free_after=free1, finite=bool(torch.isfinite(O.float()).all()))
+print("RESULT " + json.dumps(out))
+"""
+
+
+def test_noalloc_first_calls_take_no_device_memory():
+    """In a fresh process that has called nothing else of the library, the first calls of
+    the entry point (set-up included, at d = 128 and d = 64) leave the device's free memory
+    unchanged.  Modules load eagerly at context creation, so the only change a call could
+    make is an allocation of its own; cudaMalloc hands out at least 2 MiB."""
+    env = dict(os.environ, CUDA_MODULE_LOADING="EAGER")
+    r = subprocess.run([sys.executable, "-c", _FRESH_PROCESS, ROOT], env=env, capture_output=True, text=True,
+                       timeout=600)
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("RESULT ")]
+    assert r.returncode == 0 and line, r.stdout[-2000:] + r.stderr[-2000:]
+    res = json.loads(line[0][len("RESULT "):])
+    for d, v in res.items():
+        assert v["rc"] == 0 and v["finite"], (d, v)
+        assert v["free_before"] - v["free_after"] < (2 << 20), (d, v)
