@@ -143,6 +143,102 @@ def load_traffic(workload: str):
     return float(e["dram_bytes_per_launch"])
 
 
+# ------------------------------------------------------------------ NUMA placement of pinned buffers
+
+def _cpulist(text):
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def gpu_numa(dev_index):
+    """(node the GPU's PCI function reports, CPUs of that node) from sysfs, or (None, None)."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        bdf = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bdf}/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None, None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            return node, _cpulist(f.read())
+    except (OSError, ValueError, AttributeError):
+        return None, None
+
+
+def pages_nodes(addr, nbytes):
+    """NUMA nodes (and page counts) of the mapping holding [addr, addr + nbytes), read from
+    /proc/self/numa_maps and /proc/self/maps; None if not found."""
+    try:
+        spans = {}
+        with open("/proc/self/maps") as f:
+            for ln in f:
+                lo, hi = (int(x, 16) for x in ln.split()[0].split("-"))
+                spans[lo] = hi
+        with open("/proc/self/numa_maps") as f:
+            for ln in f:
+                parts = ln.split()
+                lo = int(parts[0], 16)
+                hi = spans.get(lo)
+                if hi is None or not (lo <= addr < hi):
+                    continue
+                nodes = {}
+                for tok in parts[1:]:
+                    if tok.startswith("N") and "=" in tok:
+                        k, v = tok[1:].split("=")
+                        nodes[int(k)] = int(v)
+                return nodes
+    except (OSError, ValueError):
+        return None
+    return None
+
+
+class near_gpu:
+    """Run the body with this thread bound to the CPUs of the GPU's NUMA node (those the
+    process may use), so that host memory pinned meanwhile is placed on that node."""
+
+    def __init__(self, cpus):
+        self.cpus = cpus
+        self.saved = None
+
+    def __enter__(self):
+        try:
+            allowed = os.sched_getaffinity(0)
+            use = (self.cpus or set()) & allowed
+            if use and use != allowed:
+                self.saved = allowed
+                os.sched_setaffinity(0, use)
+        except (OSError, AttributeError):
+            self.saved = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved:
+            os.sched_setaffinity(0, self.saved)
+        return False
+
+
+def h2d_rate(host, devt, stream, reps=3):
+    """GB/s of one pinned host -> device copy of `host` into `devt` (best of reps)."""
+    import torch
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            devt.copy_(host, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    return host.numel() * host.element_size() / (best * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -309,6 +405,8 @@ def parse():
     ap.add_argument("--no-variants", action="store_true", help="skip timing the lazy-rescale option")
     ap.add_argument("--path", choices=["fused", "splitkv"], default="fused")
     ap.add_argument("--layout", choices=["bhsd", "bshd", "varlen"], default="bhsd")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads of the sweep after the headline one")
     return ap.parse_args()
 
 
@@ -451,6 +549,72 @@ def copy_e2e_step(stream, ins, step, outs):
                 host.copy_(devt, non_blocking=True)
         stream.synchronize()
     return run
+
+
+# The workloads besides the headline one whose throughput the default run reports in its
+# `configs` object, each timed on its own inputs after the headline workload.
+SWEEP = ["b1h2n256d64", "causal_b4h16n2048d128", "padded_planted_b2h8n4096d128", "causal_b1h32n32768d128",
+         "causal_b1h32n32768d64"]
+
+
+def config_sweep(names, lib, pkg, stream, dev, pg, local, world, target_s=0.25):
+    """Time one attn_fwd per step on each named workload (inputs resident, CUDA events on
+    the launching stream, clocks sampled during each timed region); about target_s of
+    timed work per workload."""
+    import numpy as np
+    import torch
+    import gen
+    peak, _ = load_peaks()
+    hbm_peak, _ = load_hbm_peak()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for name in names:
+        x = gen.make_inputs(name)
+        B, H, Nq, Nk, d = x["B"], x["H"], x["Nq"], x["Nk"], x["d"]
+        lens = x["lens"]
+        dt = lambda c: torch.from_numpy(c.view(np.int16)).view(torch.bfloat16).to(dev)  # noqa: E731
+        Q, K, V = dt(x["Q"]), dt(x["K"]), dt(x["V"])
+        O = torch.empty_like(Q)
+        LSE = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        lt = None if lens is None else torch.as_tensor(lens, dtype=torch.int32, device=dev)
+        sh = ctypes.c_void_p(stream.cuda_stream)
+        a = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d, x["scale"],
+             int(x["causal"]), None if lt is None else lt.data_ptr(), sh)
+
+        def step(evs=None):
+            rc = lib.attn_fwd(*a)
+            if rc != 0:
+                raise pkg.AttnError(rc, lib.attn_last_error().decode())
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        pkg.status_sync(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        est_ms = max(e0.elapsed_time(e1) / 5, 1e-3)
+        steps = int(min(5000, max(20, target_s * 1e3 / est_ms)))
+        ms, _, clocks = timed_region(step, steps, stream, dev, pg, local)
+        pkg.status_sync(stream)
+        flops = algorithmic_flops(B, H, Nq, Nk, d, x["causal"], lens)
+        kbytes = algorithmic_bytes(B, H, Nq, Nk, d, lens)
+        tflops = world * flops / (ms * 1e-3) / 1e12
+        entry = {"ms_per_step": ms, "tflops": tflops, "frac": flops / (ms * 1e-3) / 1e12 / peak,
+                 "achieved_gbs": kbytes / (ms * 1e-3) / 1e9, "hbm_frac": kbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+                 "steps": steps, "kernel": fused_kernel_name(B, H, Nq, d, sms, x["causal"]),
+                 "flops_per_step": flops, "bytes_per_step": kbytes, "clocks": clocks,
+                 "shape": {"B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": x["causal"],
+                           "key_padding": None if lens is None else [int(v) for v in lens]}}
+        if lens is not None:
+            entry["nominal_tflops"] = tflops * algorithmic_flops(B, H, Nq, Nk, d, x["causal"]) / flops
+        out[name] = entry
+        del Q, K, V, O, LSE, lt
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -602,10 +766,26 @@ def main():
     # ---- end to end: pinned host buffers, copies in and out inside the timed region
     e2e = None
     if args.e2e_steps > 0:
+        numa = None
         if e2e_api is None:  # the host-buffer C entry point does the copies itself
-            Qh, Kh, Vh = pinned(x["Q"]), pinned(x["K"]), pinned(x["V"])
-            Oh = torch.empty_like(Qh).pin_memory()
-            Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+            # Where pinned buffers land and what that does to the host-to-device rate: one
+            # copy of Q pinned under the process's default placement, then the buffers the
+            # e2e steps use, pinned with this thread bound to the GPU's NUMA node.
+            node, node_cpus = gpu_numa(local)
+            Qd = pinned(x["Q"])
+            numa = {"gpu_numa_node": node, "process_cpus": len(os.sched_getaffinity(0)),
+                    "gpu_node_cpus_usable": len((node_cpus or set()) & os.sched_getaffinity(0)),
+                    "default_pinned_pages_by_node": pages_nodes(Qd.data_ptr(), Qd.numel() * 2),
+                    "default_h2d_gbs": h2d_rate(Qd, Q, stream)}
+            with near_gpu(node_cpus):
+                Qh, Kh, Vh = pinned(x["Q"]), pinned(x["K"]), pinned(x["V"])
+                Oh = torch.empty_like(Qh).pin_memory()
+                Lh = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+            numa.update({"e2e_pinned_pages_by_node": pages_nodes(Qh.data_ptr(), Qh.numel() * 2),
+                         "e2e_h2d_gbs": h2d_rate(Qh, Q, stream),
+                         "note": "e2e buffers pinned with the allocating thread bound to the GPU's NUMA node "
+                                 "(when the process may use its CPUs); rates are one Q-sized pinned copy"})
+            del Qd
             lh = None if lens is None else torch.as_tensor(lens, dtype=torch.int32)
 
             def e2e_step():
@@ -623,7 +803,13 @@ def main():
             h2d = sum(h.numel() for h in hosts) * 2
         e2e_s = e2e_region(e2e_step, args.e2e_steps, dev, pg)
         e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4, "ms_per_step": e2e_s * 1e3, "api": e2e_api}
+               "d2h_bytes_per_step": Oh.numel() * 2 + Lh.numel() * 4, "ms_per_step": e2e_s * 1e3, "api": e2e_api,
+               "numa": numa}
+
+    # the other workloads of the sweep, each on its own inputs, after the headline one
+    configs = None
+    if (args.path == "fused" and args.layout == "bhsd" and w["name"] == DEFAULT_WORKLOAD and not args.no_configs):
+        configs = config_sweep([n for n in SWEEP if n != w["name"]], lib, pkg, stream, dev, pg, local, world)
 
     peak, peak_src = load_peaks()
     hbm_peak, hbm_src = load_hbm_peak()
@@ -646,7 +832,8 @@ def main():
            "clocks": clocks,
            "cpu_baseline": cpu,
            "cpu_blocked": cpu_blocked,
-           "variants": variants}
+           "variants": variants,
+           "configs": configs}
     if lens is not None:  # key padding: `value` counts the valid keys; the nominal count beside it
         nominal = algorithmic_flops(B, H, Nq, Nk, d, causal)
         out["nominal"] = {"value": value * nominal / flops if flops > 0 else None, "unit": "TFLOP/s",
