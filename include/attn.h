@@ -216,7 +216,14 @@ int attn_version(void);
  *    still ends the kernel, and attn_status_sync (on a stream ordered after the call)
  *    reports it later.  check_status != 0: the call synchronises `stream` and returns
  *    ATTN_ERR_TIMEOUT if a wait ran out since the word was last read.
- *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine, and its kernels use no
+ *    local memory (which the driver would back on first launch).  Loading the library's
+ *    device code onto a device takes device memory once per process, as for any CUDA
+ *    library (the module image, which holds the fixed array): under CUDA's default lazy
+ *    module loading that happens at the library's first call on the device, whichever
+ *    entry point it is.  A caller whose device memory must not move after start-up makes
+ *    one call at start-up (attn_status_sync(NULL) is enough) or sets
+ *    CUDA_MODULE_LOADING=EAGER.
  */
 attn_status attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                              int Nq, int Nk, int d, float scale, int causal, const int32_t* key_padding_lens,

@@ -363,8 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = policy_evict_first();
       int g = 0;   // key blocks loaded so far over all items: ring slot g % kStages
       int kq = 0;  // items with work so far: uses of the Q buffer
-      int k_last[C::kStages], v_last[C::kStages];  // last load issued into each stage (-1: none)
-      for (int s = 0; s < C::kStages; ++s) k_last[s] = v_last[s] = -1;
+      // Stage st has a K (V) load in flight when bit st of k_live (v_live) is set; the bit of
+      // k_par (v_par) is the phase parity that load completes.  Bit masks rather than arrays
+      // indexed by the stage: a dynamically indexed array would live in local memory.
+      uint32_t k_live = 0, k_par = 0, v_live = 0, v_par = 0;
       bool ok = true;
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
@@ -384,13 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          k_last[st] = -1;
+          const uint32_t bit = 1u << st;
+          k_live &= ~bit;
           if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
             mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
             for (int s = 0; s < C::kSub; ++s)
               tma_load_4d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64,
                           it.k_base + (it.jb0 + j) * kBN, it.hh, it.bcoord, pol_kv);
-            k_last[st] = g;
+            k_live |= bit;
+            k_par = (k_par & ~bit) | (ph << st);
           }
           if (!mbar_wait(bar_v_free(st), ph ^ 1, wc, 2)) {
             ok = false;
@@ -400,14 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < C::kSub; ++s)
             tma_load_4d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64,
                         it.k_base + (it.jb0 + j) * kBN, it.hh, it.bcoord, pol_kv);
-          v_last[st] = g;
+          v_live |= bit;
+          v_par = (v_par & ~bit) | (ph << st);
         }
       }
       // Let the copies still in flight land before this warp leaves (in a normal run they
       // were consumed long ago; after a failed wait nobody else will wait for them).
+#pragma unroll
       for (int s = 0; s < C::kStages; ++s) {
-        if (k_last[s] >= 0) mbar_wait_drain(bar_k_full(s), (k_last[s] / C::kStages) & 1, p.timeout_ns);
-        if (v_last[s] >= 0) mbar_wait_drain(bar_v_full(s), (v_last[s] / C::kStages) & 1, p.timeout_ns);
+        if ((k_live >> s) & 1u) mbar_wait_drain(bar_k_full(s), (k_par >> s) & 1u, p.timeout_ns);
+        if ((v_live >> s) & 1u) mbar_wait_drain(bar_v_full(s), (v_par >> s) & 1u, p.timeout_ns);
       }
     }
   } else if (warp == kWarpPv || warp == kWarpS) {
@@ -770,7 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kWarpPv) {
     tc_fence_after();
-    tmem_dealloc<kTmemCols>(tmem);
+    // the base re-read from shared memory: keeping `tmem` live through every role's code
+    // to here can cost a spill (and so local memory) in the register-limited roles
+    tmem_dealloc<kTmemCols>(*reinterpret_cast<volatile uint32_t*>(tmem_slot));
   }
 }
 

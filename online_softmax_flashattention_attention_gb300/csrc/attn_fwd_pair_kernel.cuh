@@ -31,7 +31,14 @@
 
 namespace attn {
 
-constexpr int kPairThreads = 352;  // 8 softmax warps + producer + two MMA issuers
+// 8 softmax warps + producer + two MMA issuers + one warp without a role, which completes
+// the third warpgroup so that setmaxnreg can move registers from that group (producer and
+// issuers) to the softmax warps: 224 each instead of the 168 a 12-warp launch gives every
+// thread (three warps per scheduler partition of 16384 registers), with no spills.
+constexpr int kPairThreads = 384;
+constexpr uint32_t kPairRegsSoftmax = 224;
+constexpr uint32_t kPairRegsOther = 56;
+static_assert(256 * kPairRegsSoftmax + 128 * kPairRegsOther <= 168 * kPairThreads, "register split");
 constexpr int kPairWarpTma = 8;
 constexpr int kPairWarpS = 9;
 constexpr int kPairWarpPv = 10;
@@ -206,13 +213,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (warp == kPairWarpTma) {
     // ================================================================ producer
     // Warp-wide like the MMA issuers below: one elected lane issues each copy.
+    setmaxnreg_dec<kPairRegsOther>();
     {
       const uint64_t pol_kv = policy_evict_last();
       const uint64_t pol_q = policy_evict_first();
       int e = 0;   // ring entries loaded so far over all pairs (K_j, then V_j): slot e % kSlots
       int kq = 0;  // pairs with work so far: uses of the Q tiles
-      int last[C::kSlots];  // last entry loaded into each slot (-1: none pending)
-      for (int s = 0; s < C::kSlots; ++s) last[s] = -1;
+      // Slot s has a copy in flight when bit s of live is set; bit s of par is the phase
+      // parity that copy completes (bit masks: an array indexed by the slot would live in
+      // local memory).
+      uint32_t live = 0, par = 0;
       bool ok = true;
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
@@ -222,6 +232,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // the previous pair's Q tiles must have been read by its last S product
         if (kq > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13))) break;
         mbar_arrive_expect_tx_elect(bar_q_full, ((it.nblk[0] > 0) + (it.nblk[1] > 0)) * C::kTileBytes);
+#pragma unroll
         for (int t = 0; t < 2; ++t)
           if (it.nblk[t] > 0)
             tma_load_4d_elect(sQ + t * C::kTileBytes, &tmQ, bar_q_full, 0, it.q_base + it.q0[t], it.hh, it.bcoord,
@@ -234,27 +245,31 @@ __global__ void __launch_bounds__(kPairThreads, 1)
               ok = false;
               break;
             }
-            last[slot] = -1;
+            const uint32_t bit = 1u << slot;
+            live &= ~bit;
             // the test hook withholds K of one block: its full barrier never completes
             if (kv == 1 || j != p.fault_block) {
               mbar_arrive_expect_tx_elect(bar_full(slot), C::kTileBytes);
               tma_load_4d_elect(sRing + slot * C::kTileBytes, kv ? &tmV : &tmK, bar_full(slot), 0,
                                 it.k_base + j * kBN, it.hh, it.bcoord, pol_kv);
-              last[slot] = e;
+              live |= bit;
+              par = (par & ~bit) | (static_cast<uint32_t>((e / C::kSlots) & 1) << slot);
             }
           }
         }
       }
       // Let the copies still in flight land before this warp leaves (in a normal run they
       // were consumed long ago; after a failed wait nobody else will wait for them).
+#pragma unroll
       for (int s = 0; s < C::kSlots; ++s)
-        if (last[s] >= 0) mbar_wait_drain(bar_full(s), (last[s] / C::kSlots) & 1, p.timeout_ns);
+        if ((live >> s) & 1u) mbar_wait_drain(bar_full(s), (par >> s) & 1u, p.timeout_ns);
     }
   } else if (warp == kPairWarpS || warp == kPairWarpPv) {
     // ================================================================ MMA issuers
     // The whole warp runs the issuer loop (warp-uniform control flow; measured on GB300,
     // 7-9 % faster than one lane running it alone); one elected lane issues each MMA and
     // commit.
+    setmaxnreg_dec<kPairRegsOther>();
     {
       // descriptor high word: stride 1024 B, version 1, 128-byte swizzle (as attn_fwd_kernel)
       const uint32_t dhi = (1024u >> 4) | (1u << 14) | (2u << 29);
@@ -273,6 +288,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           for (int j = 0; ok && j < it.nmax; ++j, e += 2) {
             const int slot = e % C::kSlots;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_full(slot), (e / C::kSlots) & 1, wc, 5)))) break;
+#pragma unroll
             for (int t = 0; t < 2; ++t) {
               const int q = qn + 2 * j + t;
               const int b = q % kPairSBufs;
@@ -304,6 +320,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           for (int j = 0; ok && j < it.nmax; ++j, e += 2) {
             const int slot = e % C::kSlots;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_full(slot), (e / C::kSlots) & 1, wc, 7)))) break;
+#pragma unroll
             for (int t = 0; t < 2; ++t) {
               const int q = qn + 2 * j + t;
               const int b = q % kPairSBufs;
@@ -336,8 +353,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mma_commit_elect(bar_drain(di));
       mbar_wait_drain(bar_drain(di), 0, p.timeout_ns);
     }
+  } else if (warp > kPairWarpPv) {
+    setmaxnreg_dec<kPairRegsOther>();  // the warp without a role completes its warpgroup
   } else {
     // ================================================================ softmax / epilogue
+    setmaxnreg_inc<kPairRegsSoftmax>();
     const int t = warp >> 2;          // the tile these warps serve
     const int r = threadIdx.x & 127;  // row within the tile = tensor-memory lane
     const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -352,9 +372,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const PairItem it = decode_pair<kPacked>(p, item, seq_perm);
       const int qbase = qn;
       qn += 2 * it.nmax;
-      const int row = it.q0[t] + r;
+      // this tile's fields, chosen by value (an array indexed by t would go to local memory)
+      const int t_q0 = t ? it.q0[1] : it.q0[0];
+      const int t_min_limit = t ? it.min_limit[1] : it.min_limit[0];
+      const int nblk = t ? it.nblk[1] : it.nblk[0];
+      const bool t_valid = t ? it.valid[1] : it.valid[0];
+      const int row = t_q0 + r;
       const int limit = row_key_limit(row, it.kv_len, it.Nq, it.Nk, p.causal);
-      const int nblk = it.nblk[t];
       float m = -INFINITY;  // running max, log2 domain
       float l = 0.f;        // running denominator
       // Checking a barrier costs a long round trip even when its phase completed long ago,
@@ -385,7 +409,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
         for (int x = 0; x < kBN; ++x) s[x] = __uint_as_float(sr[x]);
         const int kb = j * kBN;
-        if (kb + kBN > it.min_limit[t]) {
+        if (kb + kBN > t_min_limit) {
 #pragma unroll
           for (int x = 0; x < kBN; ++x)
             if (kb + x >= limit) s[x] = -INFINITY;
@@ -441,7 +465,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           }
         };
         // blocks with a masked key (-inf scores) keep every exponential on ex2.approx
-        if (kSoftPairs > 0 && kb + kBN <= it.min_limit[t])
+        if (kSoftPairs > 0 && kb + kBN <= t_min_limit)
           exp_block(std::true_type{});
         else
           exp_block(std::false_type{});
@@ -473,7 +497,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_p_full(b));
       }
-      if (!it.valid[t]) continue;  // a tile past the end of its sequence: no rows
+      if (!t_valid) continue;  // a tile past the end of its sequence: no rows
       // ---- epilogue: one division by l; O and LSE out, straight from registers
       if (ok && nblk > 0) {
         // the tile's last P V product has landed in o~_t
@@ -526,7 +550,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __syncthreads();
   if (warp == kPairWarpPv) {
     tc_fence_after();
-    tmem_dealloc<kTmemCols>(tmem);
+    // the base re-read from shared memory: keeping `tmem` live through every role's code
+    // to here cost a spill (and so local memory) in the register-limited roles
+    tmem_dealloc<kTmemCols>(*reinterpret_cast<volatile uint32_t*>(tmem_slot));
   }
 }
 

@@ -357,6 +357,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// Per-warpgroup register budget (every warp of the warpgroup executes it): dec returns
+// registers to the CTA's pool, inc waits until the pool holds enough for it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for tcgen05 (64-bit):

@@ -88,6 +88,11 @@ sys.path.insert(0, sys.argv[1])
 import torch
 import online_softmax_flashattention_attention_gb300 as pkg
 lib = pkg.load_library()
+# Load the library's device module first (its code and the fixed array): with eager module
+# loading that happens at the library's first CUDA runtime call, a stream synchronisation
+# here, which allocates nothing itself.
+torch.cuda.init()
+assert lib.attn_status_sync(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
 f = lib.attn_fwd_noalloc
 vp, i = ctypes.c_void_p, ctypes.c_int
 f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp, i, vp]
@@ -111,10 +116,13 @@ print("RESULT " + json.dumps(out))
 
 
 def test_noalloc_first_calls_take_no_device_memory():
-    """In a fresh process that has called nothing else of the library, the first calls of
-    the entry point (set-up included, at d = 128 and d = 64) leave the device's free memory
-    unchanged.  Modules load eagerly at context creation, so the only change a call could
-    make is an allocation of its own; cudaMalloc hands out at least 2 MiB."""
+    """In a fresh process, the first calls of the entry point (set-up included, at d = 128
+    and d = 64) leave the device's free memory unchanged.  The library's device module (its
+    code and the fixed array) is loaded before the measurement, with eager module loading
+    at the library's first runtime call (a stream synchronisation); under CUDA's default
+    lazy loading that load would happen at the first call of any entry point and take one
+    2 MiB granule of device memory.  After it, the only change a call could make is an
+    allocation of its own, and cudaMalloc hands out at least 2 MiB."""
     env = dict(os.environ, CUDA_MODULE_LOADING="EAGER")
     r = subprocess.run([sys.executable, "-c", _FRESH_PROCESS, ROOT], env=env, capture_output=True, text=True,
                        timeout=600)
