@@ -320,6 +320,22 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
   return ATTN_OK;
 }
 
+// Multiplier and shift that divide by d with one multiply-high, one add and one shift:
+// n / d = (umulhi(m, n) + n) >> s for 0 <= n < 2^31 and 1 <= d < 2^31, with s = ceil(log2 d)
+// and m = floor(2^32 (2^s - d) / d) + 1 (the round-up method for division by invariant
+// integers; n + umulhi(m, n) stays below 2^32 because both terms are below 2^31).
+void divisor(int d, uint32_t* m, uint32_t* s) {
+  uint32_t l = 0;
+  while ((1ull << l) < static_cast<unsigned long long>(d)) ++l;
+  *m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - static_cast<unsigned long long>(d))) / d + 1);
+  *s = l;
+}
+void set_divisors(attn::FwdParams* p) {
+  divisor(p->num_splits, &p->dm_split, &p->ds_split);
+  divisor(p->order_div, &p->dm_order, &p->ds_order);
+  divisor(p->H, &p->dm_h, &p->ds_h);
+}
+
 // Launches `kernel` with programmatic stream serialization: it may be scheduled on the SMs
 // the previous kernel in `stream` has already left, run its prologue there (barriers,
 // tensor-memory allocation, descriptor prefetch) and wait in griddep_wait() for that
@@ -377,6 +393,7 @@ attn_status launch_one(const void* Q, const void* K, const void* V, void* O, flo
     return st;
   if (!kStates && causal && !geo.cu_q && kv_footprint(B, H, Nk, D) <= kRankMajorMaxKvBytes) p.rank_major = 1;
   p.order_div = p.rank_major ? p.BH : p.num_qtiles;
+  set_divisors(&p);
   // persistent: one CTA per SM (shared and tensor memory allow no second), each walking
   // its items
   const int sms = sm_count(dev);

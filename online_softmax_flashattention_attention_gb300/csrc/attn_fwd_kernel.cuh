@@ -87,7 +87,18 @@ struct FwdParams {
   float* st_o;             // [num_splits, BH, Nq, D] fp32 o~ (unnormalised)
   float* st_m;             // [num_splits, BH, Nq] running max of the scaled scores (natural log units)
   float* st_l;             // [num_splits, BH, Nq] running denominator
+  // The one-tile kernel's decode divides by num_splits, order_div and H as
+  // n / d = (umulhi(m, n) + n) >> s for 0 <= n < 2^31 (multiplier and shift set on the host
+  // by set_divisors): measured on GB300, 1.02-1.05x on the short-tile workloads against
+  // integer division, the same on long tiles.  (The two-tile kernel keeps the division: the
+  // same change measured 0.955x there.)
+  uint32_t dm_split, ds_split, dm_order, ds_order, dm_h, ds_h;
 };
+
+__device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
+  const uint32_t u = static_cast<uint32_t>(n);
+  return static_cast<int>((__umulhi(m, u) + u) >> s);
+}
 
 // Packed sequences are ranked by work for the item order when there are at most this many
 // (a uint16 each in shared memory); more are taken in the order of cu_seqlens.
@@ -212,18 +223,18 @@ template <bool kPacked>
 __device__ __forceinline__ Item decode(const FwdParams& p, int item, const uint16_t* seq_perm) {
   Item it;
   const int nqt = p.num_qtiles;
-  it.split = item % p.num_splits;
-  const int unit = item / p.num_splits;
+  const int unit = fast_div(item, p.dm_split, p.ds_split);
+  it.split = item - unit * p.num_splits;
   // Head major: heads in order (their K/V stay in L2 while their tiles run).  Rank major:
   // tile rank r of every head, then rank r + 1; the host picks it for causal problems
   // whose K/V all fit in L2, where the snake of item_of over every head's longest tiles
   // first evens out the CTAs' work.  Either way a head's causal tiles go longest first.
-  const int ua = unit / p.order_div;
+  const int ua = fast_div(unit, p.dm_order, p.ds_order);
   const int ub = unit - ua * p.order_div;
   it.bh = p.rank_major ? ub : ua;
   int qtile = p.rank_major ? ua : ub;
   if (p.causal) qtile = nqt - 1 - qtile;
-  it.b = it.bh / p.H;
+  it.b = fast_div(it.bh, p.dm_h, p.ds_h);
   it.hh = it.bh - it.b * p.H;
   it.q0 = qtile * kBM;
   it.q_base = 0;
