@@ -61,3 +61,32 @@ def test_kernel_label_follows_the_two_tile_rule():
     assert bench.fused_kernel_name(1, 9, 2048, 64, sms, False) == "attn_fwd_kernel<64>"      # 72 pairs
     assert bench.fused_kernel_name(1, 2, 256, 64, sms, False) == "attn_fwd_kernel<64>"
     assert bench.fused_kernel_name(2, 32, 8192, 128, sms, True) == "attn_fwd_kernel<128>"
+
+
+def test_cpulist_parsing():
+    assert bench._cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._cpulist("5") == {5}
+    assert bench._cpulist("") == set()
+
+
+def test_pages_nodes_finds_this_buffer():
+    """The NUMA report reads /proc/self/maps and numa_maps: a buffer this process has
+    touched must be found in some node (or the files are unavailable: None)."""
+    import os
+    buf = np.ones(1 << 22, dtype=np.uint8)   # 4 MiB, touched
+    nodes = bench.pages_nodes(buf.ctypes.data, buf.nbytes)
+    if not os.path.exists("/proc/self/numa_maps"):
+        assert nodes is None
+    else:
+        assert nodes is None or (isinstance(nodes, dict) and all(isinstance(k, int) for k in nodes))
+
+
+def test_near_gpu_restores_affinity():
+    import os
+    before = os.sched_getaffinity(0)
+    one = {min(before)}
+    with bench.near_gpu(one):
+        assert os.sched_getaffinity(0) == one or len(before) == 1
+    assert os.sched_getaffinity(0) == before
+    with bench.near_gpu(None):          # no node information: nothing changes
+        assert os.sched_getaffinity(0) == before

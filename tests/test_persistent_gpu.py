@@ -120,3 +120,31 @@ def test_rank_major_order_leaves_results_unchanged(d):
             Oh, Lh = run_cuda(xs, lens=[lens[b]])
             assert np.array_equal(Oh[0, 0], O[b, h]), (b, h)
             assert np.array_equal(Lh[0, 0], L[b, h]), (b, h)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,lens_kind", [
+    (128, 512, 128, 64, False, "mixed"),     # 65536 heads of one tile: bh up to 65535
+    (64, 600, 130, 128, True, None),         # 38400 heads of two tiles (the second one row)
+])
+def test_tens_of_thousands_of_heads_every_item(B, H, N, d, causal, lens_kind):
+    """Far more (batch, head) pairs than any other case: the decode's divisions by H and by
+    the item-order divisor see numerators up to 76 799.  One row of every work item is
+    compared with the oracle (a random row of the tile), plus every row of the last head."""
+    lens = None
+    if lens_kind == "mixed":
+        lens = [int(v) for v in np.random.default_rng(5).integers(0, N + 1, size=B)]
+        lens[0], lens[-1] = 0, N
+    x = custom(B, H, N, N, d, causal, seed=31 + H, lens=lens)
+    O, LSE = run_cuda(x)
+    rng = np.random.default_rng(H)
+    picks = []
+    for b in range(B):
+        for h in range(H):
+            for t0 in range(0, N, 128):
+                picks.append((b, h, int(rng.integers(t0, min(N, t0 + 128)))))
+    picks += [(B - 1, H - 1, i) for i in range(N)]
+    picks = sorted(set(picks))
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"], picks)
+    idx = tuple(np.array(picks).T)
+    compare(O[idx], LSE[idx], O_ref, LSE_ref)
+    assert np.all(np.isfinite(O))
