@@ -83,34 +83,72 @@ def test_noalloc_rejects_bad_arguments_like_attn_fwd():
 
 
 _FRESH_PROCESS = r"""
-import ctypes, json, sys
+import ctypes, ctypes.util, glob, json, os, sys
+import numpy as np
 sys.path.insert(0, sys.argv[1])
-import torch
 import online_softmax_flashattention_attention_gb300 as pkg
+
+# The CUDA runtime through ctypes rather than torch: under eager module loading torch's first
+# CUDA use would load every kernel torch ships, which takes minutes; the runtime library
+# registers no kernels of its own.
+def cudart():
+    names = [ctypes.util.find_library("cudart"), "/usr/local/cuda/lib64/libcudart.so"]
+    names += sorted(glob.glob(os.path.join(sys.prefix, "lib", "python3*", "*-packages", "nvidia", "*", "lib",
+                                           "libcudart.so*")))
+    names += sorted(glob.glob("/usr/local/lib/python3*/dist-packages/nvidia/*/lib/libcudart.so*"))
+    for n in names:
+        if n:
+            try:
+                return ctypes.CDLL(n)
+            except OSError:
+                pass
+    raise RuntimeError("no CUDA runtime library found")
+
+rt = cudart()
+vp, sz = ctypes.c_void_p, ctypes.c_size_t
+rt.cudaMalloc.argtypes = [ctypes.POINTER(vp), sz]
+rt.cudaMemcpy.argtypes = [vp, vp, sz, ctypes.c_int]
+rt.cudaMemGetInfo.argtypes = [ctypes.POINTER(sz), ctypes.POINTER(sz)]
+rt.cudaDeviceSynchronize.argtypes = []
+for f in (rt.cudaMalloc, rt.cudaMemcpy, rt.cudaMemGetInfo, rt.cudaDeviceSynchronize):
+    f.restype = ctypes.c_int
+
+def free_bytes():
+    f, t = sz(), sz()
+    assert rt.cudaDeviceSynchronize() == 0 and rt.cudaMemGetInfo(ctypes.byref(f), ctypes.byref(t)) == 0
+    return f.value
+
+def device_array(host):
+    p = vp()
+    assert rt.cudaMalloc(ctypes.byref(p), host.nbytes) == 0
+    assert rt.cudaMemcpy(p, host.ctypes.data, host.nbytes, 1) == 0   # host to device
+    return p
+
 lib = pkg.load_library()
 # Load the library's device module first (its code and the fixed array): with eager module
 # loading that happens at the library's first CUDA runtime call, a stream synchronisation
 # here, which allocates nothing itself.
-torch.cuda.init()
-assert lib.attn_status_sync(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+assert lib.attn_status_sync(None) == 0
 f = lib.attn_fwd_noalloc
-vp, i = ctypes.c_void_p, ctypes.c_int
+i = ctypes.c_int
 f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, i, vp, i, vp]
 f.restype = i
+rng = np.random.default_rng(3)
 out = {}
 for d in (128, 64):  # d = 64 with many heads takes the two-tile kernel
-    H = 2 if d == 128 else 304
-    g = torch.Generator(device="cuda").manual_seed(d)
-    Q, K, V = (torch.randn(1, H, 384, d, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
-    O = torch.empty_like(Q)
-    L = torch.empty(1, H, 384, device="cuda")
-    torch.cuda.synchronize()
-    free0 = torch.cuda.mem_get_info()[0]
-    rc = f(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(), 1, H, 384, 384, d, d ** -0.5, 1,
-           None, 1, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    torch.cuda.synchronize()
-    free1 = torch.cuda.mem_get_info()[0]
-    out[d] = dict(rc=rc, free_before=free0, free_after=free1, finite=bool(torch.isfinite(O.float()).all()))
+    H, N = (2 if d == 128 else 304), 384
+    x = (rng.standard_normal((3, 1, H, N, d)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    Q, K, V = (device_array(np.ascontiguousarray(x[t])) for t in range(3))
+    O = device_array(np.zeros((1, H, N, d), np.uint16))
+    L = device_array(np.zeros((1, H, N), np.float32))
+    free0 = free_bytes()
+    rc = f(Q, K, V, O, L, 1, H, N, N, d, d ** -0.5, 1, None, 1, None)
+    free1 = free_bytes()
+    o = np.zeros((1, H, N, d), np.uint16)
+    assert rt.cudaMemcpy(o.ctypes.data, O, o.nbytes, 2) == 0          # device to host
+    vals = (o.astype(np.uint32) << 16).view(np.float32)
+    out[d] = dict(rc=rc, free_before=free0, free_after=free1, finite=bool(np.isfinite(vals).all()),
+                  nonzero=bool((vals != 0).any()))
 print("RESULT " + json.dumps(out))
 """
 
@@ -130,5 +168,5 @@ def test_noalloc_first_calls_take_no_device_memory():
     assert r.returncode == 0 and line, r.stdout[-2000:] + r.stderr[-2000:]
     res = json.loads(line[0][len("RESULT "):])
     for d, v in res.items():
-        assert v["rc"] == 0 and v["finite"], (d, v)
+        assert v["rc"] == 0 and v["finite"] and v["nonzero"], (d, v)
         assert v["free_before"] - v["free_after"] < (2 << 20), (d, v)
