@@ -28,7 +28,8 @@ EXP2_DEFAULT, EXP2_HARDWARE, EXP2_MIXED = 0, 1, 2
 
 class AttnOptions(ctypes.Structure):
     """attn_options of include/attn.h."""
-    _fields_ = [("size", ctypes.c_size_t), ("rescale_threshold", ctypes.c_float), ("exp2_mode", ctypes.c_int)]
+    _fields_ = [("size", ctypes.c_size_t), ("rescale_threshold", ctypes.c_float), ("exp2_mode", ctypes.c_int),
+                ("key_block", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -133,13 +134,14 @@ def _outputs(Q, O, LSE):
 
 
 def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding_lens=None, stream=None,
-             rescale_threshold=0.0, exp2_mode=EXP2_DEFAULT):
+             rescale_threshold=0.0, exp2_mode=EXP2_DEFAULT, key_block=0):
     """O, LSE = softmax(scale * Q K^T + mask) V and its row logsumexp, on the GPU.
 
     Q [B,H,Nq,d], K/V [B,H,Nk,d]: contiguous bf16 CUDA tensors.  O (bf16) and LSE
     (fp32 [B,H,Nq]) are allocated when not given.  key_padding_lens: int32 CUDA
     tensor [B] or None.  Enqueued on ``stream`` (default: torch's current stream).
-    rescale_threshold / exp2_mode: the attn_options of attn_fwd_ex (defaults: attn_fwd).
+    rescale_threshold / exp2_mode / key_block: the attn_options of attn_fwd_ex (defaults:
+    attn_fwd).
     """
     import torch
     B, H, Nq, d = Q.shape
@@ -164,11 +166,11 @@ def attn_fwd(Q, K, V, O=None, LSE=None, *, scale=None, causal=False, key_padding
         if key_padding_lens.dtype != torch.int32 or not key_padding_lens.is_cuda or key_padding_lens.numel() != B:
             raise ValueError("key_padding_lens must be an int32 CUDA tensor [B]")
         lens_ptr = key_padding_lens.data_ptr()
-    if rescale_threshold == 0.0 and exp2_mode == EXP2_DEFAULT:
+    if rescale_threshold == 0.0 and exp2_mode == EXP2_DEFAULT and key_block == 0:
         rc = attn_fwd_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H, Nq, Nk, d,
                           float(scale), causal, lens_ptr, _stream_handle(stream))
     else:
-        opts = AttnOptions(ctypes.sizeof(AttnOptions), float(rescale_threshold), int(exp2_mode))
+        opts = AttnOptions(ctypes.sizeof(AttnOptions), float(rescale_threshold), int(exp2_mode), int(key_block))
         rc = load_library().attn_fwd_ex(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(), B, H,
                                         Nq, Nk, d, float(scale), int(causal), lens_ptr, ctypes.byref(opts),
                                         _stream_handle(stream))

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -163,12 +164,13 @@ Geometry dense_geometry(int B, int H, int Nq, int Nk, int d) {
 
 // 4-D map (d, rows, H, B) over bf16 with element strides (batch, head, row), box
 // (64, 128, 1, 1), 128-byte swizzle; rows past `rows` read as zero and are not stored.
-attn_status make_map(CUtensorMap* map, const void* ptr, int d, long long rows, int H, int B, const long long* st) {
+attn_status make_map(CUtensorMap* map, const void* ptr, int d, long long rows, int H, int B, const long long* st,
+                     int box_rows = attn::kBM) {
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
                            static_cast<cuuint64_t>(st[0]) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -245,6 +247,7 @@ constexpr int kDefaultSoftPairs = (D == 128) ? ATTN_SOFT_PAIRS_D128 : ATTN_SOFT_
 struct Variant {
   float tau_log2 = 0.f;  // rescale threshold in log2 units
   bool soft = false;     // mixed exponentials (kDefaultSoftPairs) or ex2.approx only (default)
+  int key_block = attn::kBN;  // keys per block: kBN, or kBNWide (d = 128 dense, O out)
 };
 
 // Sets max dynamic shared memory once per device for a kernel instantiation.
@@ -265,7 +268,7 @@ template <int D, bool kStates>
 attn_status make_launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                         int Nk, float scale, int causal, const int32_t* lens, uint32_t* status, const StateOut& so,
                         const Variant& var, const Geometry& geo, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
-                        CUtensorMap* mo, attn::FwdParams* pp) {
+                        CUtensorMap* mo, attn::FwdParams* pp, int kv_box_rows = attn::kBN) {
   const int BH = B * H;
   attn_status st;
   if ((st = make_map(mq, Q, D, geo.q_rows, H, geo.map_b, geo.qs)) != ATTN_OK) return st;
@@ -275,8 +278,9 @@ attn_status make_launch(const void* Q, const void* K, const void* V, void* O, fl
     return st;
   }
   if (geo.k_rows > 0) {
-    if ((st = make_map(mk, K, D, geo.k_rows, H, geo.map_b, geo.ks)) != ATTN_OK) return st;
-    if ((st = make_map(mv, V, D, geo.k_rows, H, geo.map_b, geo.vs)) != ATTN_OK) return st;
+    // K and V move a key block at a time: kv_box_rows rows per copy
+    if ((st = make_map(mk, K, D, geo.k_rows, H, geo.map_b, geo.ks, kv_box_rows)) != ATTN_OK) return st;
+    if ((st = make_map(mv, V, D, geo.k_rows, H, geo.map_b, geo.vs, kv_box_rows)) != ATTN_OK) return st;
   } else {  // never read: every row is fully masked
     *mk = *mq;
     *mv = *mq;
@@ -367,10 +371,11 @@ long long kv_footprint(int B, int H, int Nk, int D) { return 4ll * B * H * Nk * 
 
 // The shared-memory attribute of one instantiation of each forward kernel, set once per
 // device (one flag per device and instantiation).
-template <int D, bool kStates, int kSoft, bool kPacked>
+template <int D, bool kStates, int kSoft, bool kPacked, int BN = attn::kBN>
 attn_status fwd_kernel_attr(int dev) {
   static bool attr_set[kMaxDevices] = {};
-  return set_smem_attr(attn::attn_fwd_kernel<D, kStates, kSoft, kPacked>, attn::FwdCfg<D>::kSmemAlloc, dev, attr_set);
+  return set_smem_attr(attn::attn_fwd_kernel<D, kStates, kSoft, kPacked, BN>, attn::FwdCfg<D, BN>::kSmemAlloc, dev,
+                       attr_set);
 }
 template <int kSoft, bool kPacked>
 attn_status pair_kernel_attr(int dev) {
@@ -378,18 +383,18 @@ attn_status pair_kernel_attr(int dev) {
   return set_smem_attr(attn::attn_fwd_pair_kernel<kSoft, kPacked>, attn::PairCfg::kSmemAlloc, dev, attr_set);
 }
 
-template <int D, bool kStates, int kSoft, bool kPacked>
+template <int D, bool kStates, int kSoft, bool kPacked, int BN = attn::kBN>
 attn_status launch_one(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq,
                        int Nk, float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev,
                        uint32_t* status, const StateOut& so, const Variant& var, const Geometry& geo) {
-  using C = attn::FwdCfg<D>;
-  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft, kPacked>;
+  using C = attn::FwdCfg<D, BN>;
+  auto kernel = attn::attn_fwd_kernel<D, kStates, kSoft, kPacked, BN>;
   attn_status st;
-  if ((st = fwd_kernel_attr<D, kStates, kSoft, kPacked>(dev)) != ATTN_OK) return st;
+  if ((st = fwd_kernel_attr<D, kStates, kSoft, kPacked, BN>(dev)) != ATTN_OK) return st;
   CUtensorMap mq, mk, mv, mo;
   attn::FwdParams p;
   if ((st = make_launch<D, kStates>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens, status, so, var, geo, &mq,
-                                    &mk, &mv, &mo, &p)) != ATTN_OK)
+                                    &mk, &mv, &mo, &p, BN)) != ATTN_OK)
     return st;
   if (!kStates && causal && !geo.cu_q && kv_footprint(B, H, Nk, D) <= kRankMajorMaxKvBytes) p.rank_major = 1;
   p.order_div = p.rank_major ? p.BH : p.num_qtiles;
@@ -445,6 +450,13 @@ template <int D, bool kStates, bool kPacked>
 attn_status launch_as(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
                       float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
                       const StateOut& so, const Variant& var, const Geometry& g) {
+  if (var.key_block == attn::kBNWide) {  // the 192-key-block build: d = 128, O out, not packed
+    if constexpr (D == 128 && !kStates && !kPacked)
+      return launch_one<128, false, 0, false, attn::kBNWide>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens,
+                                                             stream, dev, status, so, var, g);
+    return fail(ATTN_ERR_BAD_ARG, "key_block=%d is available at d = 128 without packed sequences",
+                attn::kBNWide);
+  }
   if constexpr (D == 64 && !kStates) {
     if (use_pair_kernel(dev, B, H, g, causal)) {
       if (var.soft)
@@ -479,8 +491,11 @@ attn_status launch(const void* Q, const void* K, const void* V, void* O, float* 
 attn_status resolve_options(const attn_options* opts, Variant* var) {
   *var = Variant{};
   if (!opts) return ATTN_OK;
-  if (opts->size < sizeof(attn_options))
-    return fail(ATTN_ERR_BAD_ARG, "attn_options.size=%zu; expected %zu", opts->size, sizeof(attn_options));
+  // the first fields are always there; key_block was added later and defaults when the
+  // caller's struct ends before it
+  const size_t base = offsetof(attn_options, key_block);
+  if (opts->size < base)
+    return fail(ATTN_ERR_BAD_ARG, "attn_options.size=%zu; expected at least %zu", opts->size, base);
   const float t = opts->rescale_threshold;
   if (!std::isfinite(t) || t < 0.f || t > 20.f)
     return fail(ATTN_ERR_BAD_ARG, "rescale_threshold=%g; must be in [0, 20]", static_cast<double>(t));
@@ -488,6 +503,14 @@ attn_status resolve_options(const attn_options* opts, Variant* var) {
     return fail(ATTN_ERR_BAD_ARG, "exp2_mode=%d", opts->exp2_mode);
   var->tau_log2 = static_cast<float>(static_cast<double>(t) * 1.4426950408889634);
   var->soft = opts->exp2_mode == ATTN_EXP2_MIXED;
+  if (opts->size >= base + sizeof(int)) {
+    const int kb = opts->key_block;
+    if (kb != 0 && kb != attn::kBN && kb != attn::kBNWide)
+      return fail(ATTN_ERR_BAD_ARG, "key_block=%d; must be 0, %d or %d", kb, attn::kBN, attn::kBNWide);
+    if (kb == attn::kBNWide && var->soft)
+      return fail(ATTN_ERR_BAD_ARG, "key_block=%d takes exp2_mode ATTN_EXP2_HARDWARE or DEFAULT", kb);
+    var->key_block = kb == 0 ? attn::kBN : kb;
+  }
   return ATTN_OK;
 }
 

@@ -46,8 +46,8 @@
 namespace attn {
 
 constexpr int kBM = 128;           // query rows per tile (= tensor-memory lanes)
-constexpr int kBN = 128;           // keys per block
-constexpr int kSBufs = 3;          // tensor-memory score buffers
+constexpr int kBN = 128;           // keys per block (kBNWide: the d = 128 option of attn_fwd_ex)
+constexpr int kBNWide = 192;
 constexpr int kWarpTma = 4;
 constexpr int kWarpPv = 5;
 constexpr int kWarpS = 6;
@@ -104,23 +104,34 @@ __device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
 // (a uint16 each in shared memory); more are taken in the order of cu_seqlens.
 constexpr int kMaxSortedSeqs = 512;
 
-template <int D>
+// BN: keys per block.  128 everywhere by default.  At d = 128 a forward with O out can take
+// 192-key blocks instead (attn_fwd_ex, key_block = 192): tensor memory then holds two score
+// buffers of 192 columns and o~ (512 columns), shared memory Q and two K/V stages of 48 KB.
+// Measured on GB300 it is slower (two score buffers leave the softmax warps waiting for
+// scores); it stays as an option because it is the same recurrence over other blocks, which
+// a test compares with the 128-key build.
+template <int D, int BN = kBN>
 struct FwdCfg {
-  static constexpr int kSub = D / 64;                 // 64-column swizzle sub-tiles per row tile
-  static constexpr int kSubBytes = 128 * 128;         // 128 rows x 64 bf16 = 16 KiB
-  static constexpr int kTileBytes = kSub * kSubBytes; // 128 rows x D bf16
-  static constexpr int kStages = (D == 128) ? 3 : 4;  // K/V ring depth
+  static constexpr int kBNc = BN;
+  static constexpr int kSub = D / 64;                   // 64-column swizzle sub-tiles per row tile
+  static constexpr int kSubBytesQ = kBM * 128;          // 128 rows x 64 bf16 = 16 KiB
+  static constexpr int kSubBytesKV = BN * 128;          // BN rows x 64 bf16
+  static constexpr int kQBytes = kSub * kSubBytesQ;     // 128 rows x D bf16
+  static constexpr int kKVBytes = kSub * kSubBytesKV;   // BN rows x D bf16
+  static constexpr int kStages = BN != kBN ? 2 : (D == 128) ? 3 : 4;  // K/V ring depth
+  static constexpr int kSBufs = BN != kBN ? 2 : 3;      // tensor-memory score buffers
   // How a tile's O leaves (measured on GB300): at d = 64 it is staged in the V stage of the
   // tile's last block and stored by TMA (a 16 KB tile in a 4-deep ring); at d = 128 the
   // stage would take a third of the ring while the store reads it, so each thread stores
   // its row straight from registers.
   static constexpr bool kStageO = (D == 64);
+  static_assert(!kStageO || BN == kBM, "O is staged in a V stage of the tile's own size");
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kStages * kKVBytes;
   // barriers: q_full, q_free, (one unused slot), k_full[S], v_full[S], k_free[S],
-  // v_free[S], s_full[3], pv_done[3], p_full[3], drain[2]
+  // v_free[S], s_full[B], pv_done[B], p_full[B], drain[2]
   static constexpr int kNumBars = 3 + 4 * kStages + 3 * kSBufs + 2;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
   static constexpr int kOffPerm = kOffMisc + 16;           // uint16 order of packed sequences
@@ -128,11 +139,11 @@ struct FwdCfg {
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack to align the base to 1024 B
   static constexpr int kSmemAllocNoPerm = kOffPerm + 1024; // launches without seq_sort
   static_assert(kSmemAlloc <= 232448, "shared memory per CTA");
-  static_assert(kTileBytes >= 4 * kMaxSortedSeqs, "the Q tile holds rank_sequences' scratch");
-  // tensor-memory columns: S buffers b = 0..2 (P aliases the first 64 columns), then o~
-  __host__ __device__ static constexpr uint32_t col_s(int b) { return 128u * b; }
-  static constexpr uint32_t kColO = 128u * kSBufs;
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, 0);
+  static_assert(kQBytes >= 4 * kMaxSortedSeqs, "the Q tile holds rank_sequences' scratch");
+  // tensor-memory columns: S buffers b (P aliases the first BN / 2 columns), then o~
+  __host__ __device__ static constexpr uint32_t col_s(int b) { return static_cast<uint32_t>(BN) * b; }
+  static constexpr uint32_t kColO = static_cast<uint32_t>(BN) * kSBufs;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, BN, 0);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(kBM, D, 1);
   static_assert(kColO + D <= kTmemCols, "tensor memory");
 };
@@ -219,7 +230,7 @@ __device__ __noinline__ void rank_sequences(const FwdParams& p, int B, float* sc
 
 // kPacked: a launch over packed sequences (cu_q set), which may take them in the order of
 // seq_perm; the other launches' code has no such step.
-template <bool kPacked>
+template <bool kPacked, int BN>
 __device__ __forceinline__ Item decode(const FwdParams& p, int item, const uint16_t* seq_perm) {
   Item it;
   const int nqt = p.num_qtiles;
@@ -269,7 +280,7 @@ __device__ __forceinline__ Item decode(const FwdParams& p, int item, const uint1
   const int qlast = min(it.q0 + kBM - 1, it.Nq - 1);
   const int max_limit = row_key_limit(qlast, it.kv_len, it.Nq, it.Nk, p.causal);
   it.min_limit = row_key_limit(it.q0, it.kv_len, it.Nq, it.Nk, p.causal);
-  const int nvis = max_limit > 0 ? (max_limit + kBN - 1) / kBN : 0;  // key blocks any row of the tile sees
+  const int nvis = max_limit > 0 ? (max_limit + BN - 1) / BN : 0;  // key blocks any row of the tile sees
   // without splits an item takes every visible block (its key count may be per sequence)
   it.jb0 = it.split * p.split_blocks;
   const int nsplit = p.num_splits > 1 ? max(0, min(nvis, it.jb0 + p.split_blocks) - it.jb0) : nvis;
@@ -294,12 +305,14 @@ __device__ __forceinline__ int item_of(int r, int c, int G) { return r * G + ((r
 // P V product has finished, and leaves by one TMA store; the softmax warps then hand that
 // stage back to the producer (v_free) instead of the P V issuer.  At d = 128 each thread
 // stores its row of O straight from registers.
-template <int D, bool kStates, int kSoftPairs, bool kPacked>
+template <int D, bool kStates, int kSoftPairs, bool kPacked, int BN = kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, BN>;
+  constexpr int kBN = BN;           // keys per block of this instantiation
+  constexpr int kSBufs = C::kSBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -382,13 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ri = 0; ok; ++ri) {
         const int item = item_of(ri, cta, G);
         if (item >= p.num_items) break;
-        const Item it = decode<kPacked>(p, item, seq_perm);
+        const Item it = decode<kPacked, kBN>(p, item, seq_perm);
         if (it.nblk == 0) continue;
         // the previous tile's Q must have been read by its last S product
         if (kq > 0 && !mbar_wait(bar_q_free, (kq - 1) & 1, wc, 13)) break;
-        mbar_arrive_expect_tx(bar_q_full, C::kTileBytes);
+        mbar_arrive_expect_tx(bar_q_full, C::kQBytes);
         for (int s = 0; s < C::kSub; ++s)
-          tma_load_4d(sQ + s * C::kSubBytes, &tmQ, bar_q_full, s * 64, it.q_base + it.q0, it.hh, it.bcoord, pol_q);
+          tma_load_4d(sQ + s * C::kSubBytesQ, &tmQ, bar_q_full, s * 64, it.q_base + it.q0, it.hh, it.bcoord, pol_q);
         ++kq;
         for (int j = 0; j < it.nblk; ++j, ++g) {
           const int st = g % C::kStages;
@@ -400,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bit = 1u << st;
           k_live &= ~bit;
           if (j != p.fault_block) {  // the test hook withholds one block: its k_full never completes
-            mbar_arrive_expect_tx(bar_k_full(st), C::kTileBytes);
+            mbar_arrive_expect_tx(bar_k_full(st), C::kKVBytes);
             for (int s = 0; s < C::kSub; ++s)
-              tma_load_4d(sK + st * C::kTileBytes + s * C::kSubBytes, &tmK, bar_k_full(st), s * 64,
+              tma_load_4d(sK + st * C::kKVBytes + s * C::kSubBytesKV, &tmK, bar_k_full(st), s * 64,
                           it.k_base + (it.jb0 + j) * kBN, it.hh, it.bcoord, pol_kv);
             k_live |= bit;
             k_par = (k_par & ~bit) | (ph << st);
@@ -411,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar_v_full(st), C::kTileBytes);
+          mbar_arrive_expect_tx(bar_v_full(st), C::kKVBytes);
           for (int s = 0; s < C::kSub; ++s)
-            tma_load_4d(sV + st * C::kTileBytes + s * C::kSubBytes, &tmV, bar_v_full(st), s * 64,
+            tma_load_4d(sV + st * C::kKVBytes + s * C::kSubBytesKV, &tmV, bar_v_full(st), s * 64,
                         it.k_base + (it.jb0 + j) * kBN, it.hh, it.bcoord, pol_kv);
           v_live |= bit;
           v_par = (v_par & ~bit) | (ph << st);
@@ -443,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ri = 0; ok; ++ri) {
           const int item = item_of(ri, cta, G);
           if (item >= p.num_items) break;
-          const Item it = decode<kPacked>(p, item, seq_perm);
+          const Item it = decode<kPacked, kBN>(p, item, seq_perm);
           if (it.nblk == 0) continue;
           ok = mbar_wait(bar_q_full, kq & 1, wc, 3);
           for (int j = 0; ok && j < it.nblk; ++j, ++g) {
@@ -455,13 +468,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             // S_g = Q K_g^T: 8 (d = 128) or 4 (d = 64) k-steps of 16
-            const uint32_t blo = klo + st * (C::kTileBytes >> 4);
+            const uint32_t blo = klo + st * (C::kKVBytes >> 4);
             const uint32_t dst = tmem + C::col_s(bf);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t off = (ks / 4) * (C::kSubBytes >> 4) + (ks % 4) * 2;
-              mma_ss(dst, (static_cast<uint64_t>(dhi) << 32) | (qlo + off),
-                     (static_cast<uint64_t>(dhi) << 32) | (blo + off), C::kIdescS, ks > 0 ? 1u : 0u);
+              // k-step ks: 16 columns of d, in sub-tile ks / 4 of the Q and of the K tile
+              const uint32_t offq = (ks / 4) * (C::kSubBytesQ >> 4) + (ks % 4) * 2;
+              const uint32_t offk = (ks / 4) * (C::kSubBytesKV >> 4) + (ks % 4) * 2;
+              mma_ss(dst, (static_cast<uint64_t>(dhi) << 32) | (qlo + offq),
+                     (static_cast<uint64_t>(dhi) << 32) | (blo + offk), C::kIdescS, ks > 0 ? 1u : 0u);
             }
             mma_commit(bar_s_full(bf));
             mma_commit(bar_k_free(st));
@@ -471,11 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kq;
         }
       } else {
-        const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytes >> 4) << 16);
+        const uint32_t vlo = (sV >> 4) | (static_cast<uint32_t>(C::kSubBytesKV >> 4) << 16);
         for (int ri = 0; ok; ++ri) {
           const int item = item_of(ri, cta, G);
           if (item >= p.num_items) break;
-          const Item it = decode<kPacked>(p, item, seq_perm);
+          const Item it = decode<kPacked, kBN>(p, item, seq_perm);
           if (it.nblk == 0) continue;
           // The first product of a tile overwrites o~.  The softmax warps read the previous
           // tile's o~ out before they write this tile's first P, and P_0 is awaited below,
@@ -488,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             // o~ += P_g V_g: 8 k-steps of 16 keys; A = P_g from tensor memory, B = V_g MN-major
-            const uint32_t blo = vlo + st * (C::kTileBytes >> 4);
+            const uint32_t blo = vlo + st * (C::kKVBytes >> 4);
             const uint32_t a = tmem + C::col_s(g % kSBufs);
 #pragma unroll
             for (int ks = 0; ks < kBN / 16; ++ks)
@@ -518,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const int item = item_of(ri, cta, G);
       if (item >= p.num_items) break;
-      const Item it = decode<kPacked>(p, item, seq_perm);
+      const Item it = decode<kPacked, kBN>(p, item, seq_perm);
       if (!it.valid) continue;  // a tile past the end of a shorter packed sequence
       const int row = it.q0 + r;
       const int limit = row_key_limit(row, it.kv_len, it.Nq, it.Nk, p.causal);
@@ -582,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < kBN / 32; ++q) {
             if (q == kBN / 32 - 1)
               s_seen = j + 1 < nblk && mbar_test_wait(bar_s_full((gj + 1) % kSBufs), ((gj + 1) / kSBufs) & 1);
-            if (q == 3)
+            if (q == kBN / 32 - 1)
               pv_seen = j > 0 && mbar_test_wait(bar_pv_done((gj - 1) % kSBufs), ((gj - 1) / kSBufs) & 1);
             uint32_t pk[16];
 #pragma unroll
@@ -659,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int st_last = gl % C::kStages;
-        const uint32_t stage = sV + st_last * C::kTileBytes;
+        const uint32_t stage = sV + st_last * C::kKVBytes;
         uint8_t* orow = smem + (stage - sbase) + r * 128;
         // the last tile of a packed sequence would overrun into the next sequence under a
         // TMA store: its rows are stored one by one instead (the same for the whole CTA)
@@ -685,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // columns 32q .. 32q + 31 = four 16-byte chunks of sub-tile q / 2, chunk
               // (q % 2) * 4 + ch, 128-byte swizzle
               const int chunk = (q % 2) * 4 + ch;
-              *reinterpret_cast<uint4*>(orow + (q / 2) * C::kSubBytes + ((chunk ^ (r & 7)) * 16)) = v;
+              *reinterpret_cast<uint4*>(orow + (q / 2) * C::kSubBytesKV + ((chunk ^ (r & 7)) * 16)) = v;
             }
           }
         }
@@ -700,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r == 0) {
           if (!direct) {
             for (int s = 0; s < C::kSub; ++s)
-              tma_store_4d(&tmO, stage + s * C::kSubBytes, s * 64, it.q_base + it.q0, it.hh, it.bcoord);
+              tma_store_4d(&tmO, stage + s * C::kSubBytesKV, s * 64, it.q_base + it.q0, it.hh, it.bcoord);
             tma_store_commit();
             tma_store_wait_read();  // the stage may be loaded again once the store has read it
           }

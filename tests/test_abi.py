@@ -125,7 +125,7 @@ def test_splitkv_workspace_checks(lib):
 
 def test_options_struct_checks(lib):
     def call(**kw):
-        o = pkg.AttnOptions(ctypes.sizeof(pkg.AttnOptions), kw.get("tau", 0.0), kw.get("mode", 0))
+        o = pkg.AttnOptions(ctypes.sizeof(pkg.AttnOptions), kw.get("tau", 0.0), kw.get("mode", 0), kw.get("kb", 0))
         if "size" in kw:
             o.size = kw["size"]
         return lib.attn_fwd_ex(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, 256, 256, 64, 0.125, 0, None,
@@ -136,7 +136,13 @@ def test_options_struct_checks(lib):
     assert call(tau=float("nan")) == -8
     assert call(mode=3) == -8
     assert call(mode=-1) == -8
-    assert ctypes.sizeof(pkg.AttnOptions) == 16
+    assert call(kb=64) == -8                 # keys per block: 0, 128 or 192
+    assert call(kb=192, mode=2) == -8        # the 192-key build takes the hardware exponentials
+    # a struct that ends before key_block (its size was 16 bytes) is still accepted: the
+    # call gets past the options (and fails later only for want of a GPU here)
+    assert call(size=16) != -8
+    assert call(kb=192) != -8
+    assert ctypes.sizeof(pkg.AttnOptions) == 24
 
 
 def test_exp2_polynomial_bound():

@@ -37,7 +37,7 @@ def custom(B, H, Nq, Nk, d, causal=False, seed=7, lens=None, qk=("normal", 0.0, 
     return gen.make_inputs(w)
 
 
-def run_ex(x, tau, mode, Q=None, K=None, V=None, lens=None, Nk=None):
+def run_ex(x, tau, mode, Q=None, K=None, V=None, lens=None, Nk=None, key_block=0):
     import torch
     pkg = _pkg()
     Q = to_device(x["Q"]) if Q is None else Q
@@ -49,7 +49,7 @@ def run_ex(x, tau, mode, Q=None, K=None, V=None, lens=None, Nk=None):
     lens = x["lens"] if lens is None else lens
     lt = None if lens is None else torch.as_tensor(np.asarray(lens, np.int32)).cuda()
     pkg.attn_fwd(Q, K, V, O, LSE, scale=x["scale"], causal=x["causal"], key_padding_lens=lt,
-                 rescale_threshold=tau, exp2_mode=mode)
+                 rescale_threshold=tau, exp2_mode=mode, key_block=key_block)
     pkg.status_sync()
     return O.float().cpu().numpy().astype(np.float64), LSE.cpu().numpy().astype(np.float64)
 
@@ -171,3 +171,58 @@ def test_largest_threshold_with_values_of_100():
         assert np.all(np.isfinite(O)) and np.all(np.isfinite(LSE))
         O_ref, LSE_ref = oracle.attention(q, k, v, 1.0, False, None)
         compare(O, LSE, O_ref, LSE_ref, s_v=100.0)
+
+
+# ------------------------------------------------------------------ key-block size
+
+WIDE_SHAPES = [
+    (2, 3, 300, 300, True, None),
+    (3, 1, 260, 700, False, [0, 1, 700]),
+    (1, 2, 200, 383, True, None),             # Nq < Nk, bottom-right causal
+    (1, 2, 383, 200, True, None),             # Nq > Nk: first rows fully masked
+    (2, 2, 640, 1000, False, [1000, 191]),    # padding inside the first and the sixth block
+    (2, 40, 300, 600, True, None),            # more items than SMs
+]
+
+
+@pytest.mark.parametrize("shape", WIDE_SHAPES)
+def test_key_block_192_matches_128_and_oracle(shape):
+    """The recurrence's result does not depend on the key-block size ("FlashAttention
+    math", "Proof of exactness"; "Tiled attention: running max softmax" varies the tile):
+    the 192-key build agrees with the oracle and with the 128-key build within the
+    tolerance, with the pages' rescale rule and with the lazy option."""
+    B, H, Nq, Nk, causal, lens = shape
+    x = custom(B, H, Nq, Nk, 128, causal, seed=Nq + Nk + 5, lens=lens)
+    O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"])
+    for tau in (0.0, 5.5):
+        O128, L128 = run_ex(x, tau, 1)
+        O192, L192 = run_ex(x, tau, 1, key_block=192)
+        compare(O192, L192, O_ref, LSE_ref)
+        compare(O192, L192, O128, L128)
+
+
+def test_key_block_192_full_size_every_item():
+    """B4 H16 N2048 d128 causal with 192-key blocks: two rows of every work item against the
+    oracle, and every row against the 128-key build."""
+    x = gen.make_inputs("causal_b4h16n2048d128")
+    O192, L192 = run_ex(x, 0.0, 1, key_block=192)
+    O128, L128 = run_ex(x, 0.0, 1)
+    compare(O192, L192, O128, L128)
+    rng = np.random.default_rng(12)
+    picks = sorted({p for b in range(4) for h in range(16) for t0 in range(0, 2048, 128)
+                    for p in ((b, h, int(rng.integers(t0, t0 + 128))), (b, h, t0 + 127))})
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], True, None, picks)
+    idx = tuple(np.array(picks).T)
+    compare(O192[idx], L192[idx], O_ref, LSE_ref)
+
+
+def test_key_block_192_rejected_where_not_built():
+    pkg = _pkg()
+    x = custom(1, 2, 256, 256, 64, False, seed=3)
+    with pytest.raises(pkg.AttnError) as err:
+        run_ex(x, 0.0, 1, key_block=192)          # d = 64
+    assert err.value.status == -8
+    x = custom(1, 2, 256, 256, 128, False, seed=4)
+    with pytest.raises(pkg.AttnError) as err:
+        run_ex(x, 0.0, 2, key_block=192)          # mixed exponentials
+    assert err.value.status == -8
