@@ -108,13 +108,15 @@ typedef struct attn_options {
    * excluded.  Example: at tau = 20 and Nk = 2^20 keys, |V| must stay below 6.7e23. */
   float rescale_threshold;
   int exp2_mode;           /* ATTN_EXP2_* */
-  /* Keys per block: 0 or 128 (the default) or 192.  192 is available at d = 128 for the
-   * dense layouts (attn_fwd_ex; not packed sequences, not split-KV states) with exp2_mode
-   * DEFAULT or HARDWARE: the same recurrence over 192-key blocks ("FlashAttention math",
-   * "Proof of exactness": blocks of any size give the same result), with two score buffers
-   * in tensor memory instead of three.  Measured slower than 128 on GB300 (0.86-0.96x); it
-   * lets a caller check that the result does not depend on the block size.  Callers built
-   * before this field existed pass a smaller size and get the default. */
+  /* Keys per block: 0 or 128 (the default), 64 or 192.  64 and 192 are available at
+   * d = 128 for the dense layouts (attn_fwd_ex; not packed sequences, not split-KV states)
+   * with exp2_mode DEFAULT or HARDWARE: the same recurrence over blocks of another size
+   * ("FlashAttention math", "Proof of exactness": blocks of any size give the same result).
+   * 192 keeps two score buffers in tensor memory instead of three, 64 three buffers of 64
+   * columns and four K/V stages.  Both are measured slower than 128 on GB300; they let a
+   * caller check that the result does not depend on the block size.  Any other value is
+   * ATTN_ERR_BAD_ARG.  Callers built before this field existed pass a smaller size and get
+   * the default. */
   int key_block;
 } attn_options;
 

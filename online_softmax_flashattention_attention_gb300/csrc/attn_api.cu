@@ -247,7 +247,7 @@ constexpr int kDefaultSoftPairs = (D == 128) ? ATTN_SOFT_PAIRS_D128 : ATTN_SOFT_
 struct Variant {
   float tau_log2 = 0.f;  // rescale threshold in log2 units
   bool soft = false;     // mixed exponentials (kDefaultSoftPairs) or ex2.approx only (default)
-  int key_block = attn::kBN;  // keys per block: kBN, or kBNWide (d = 128 dense, O out)
+  int key_block = attn::kBN;  // keys per block: kBN, or kBNWide / kBNNarrow (d = 128 dense, O out)
 };
 
 // Sets max dynamic shared memory once per device for a kernel instantiation.
@@ -450,12 +450,16 @@ template <int D, bool kStates, bool kPacked>
 attn_status launch_as(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int Nq, int Nk,
                       float scale, int causal, const int32_t* lens, cudaStream_t stream, int dev, uint32_t* status,
                       const StateOut& so, const Variant& var, const Geometry& g) {
-  if (var.key_block == attn::kBNWide) {  // the 192-key-block build: d = 128, O out, not packed
-    if constexpr (D == 128 && !kStates && !kPacked)
-      return launch_one<128, false, 0, false, attn::kBNWide>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens,
-                                                             stream, dev, status, so, var, g);
+  if (var.key_block != attn::kBN) {  // the 192- and 64-key-block builds: d = 128, O out, not packed
+    if constexpr (D == 128 && !kStates && !kPacked) {
+      if (var.key_block == attn::kBNWide)
+        return launch_one<128, false, 0, false, attn::kBNWide>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens,
+                                                               stream, dev, status, so, var, g);
+      return launch_one<128, false, 0, false, attn::kBNNarrow>(Q, K, V, O, LSE, B, H, Nq, Nk, scale, causal, lens,
+                                                               stream, dev, status, so, var, g);
+    }
     return fail(ATTN_ERR_BAD_ARG, "key_block=%d is available at d = 128 without packed sequences",
-                attn::kBNWide);
+                var.key_block);
   }
   if constexpr (D == 64 && !kStates) {
     if (use_pair_kernel(dev, B, H, g, causal)) {
@@ -505,9 +509,10 @@ attn_status resolve_options(const attn_options* opts, Variant* var) {
   var->soft = opts->exp2_mode == ATTN_EXP2_MIXED;
   if (opts->size >= base + sizeof(int)) {
     const int kb = opts->key_block;
-    if (kb != 0 && kb != attn::kBN && kb != attn::kBNWide)
-      return fail(ATTN_ERR_BAD_ARG, "key_block=%d; must be 0, %d or %d", kb, attn::kBN, attn::kBNWide);
-    if (kb == attn::kBNWide && var->soft)
+    if (kb != 0 && kb != attn::kBN && kb != attn::kBNWide && kb != attn::kBNNarrow)
+      return fail(ATTN_ERR_BAD_ARG, "key_block=%d; must be 0, %d, %d or %d", kb, attn::kBN, attn::kBNNarrow,
+                  attn::kBNWide);
+    if ((kb == attn::kBNWide || kb == attn::kBNNarrow) && var->soft)
       return fail(ATTN_ERR_BAD_ARG, "key_block=%d takes exp2_mode ATTN_EXP2_HARDWARE or DEFAULT", kb);
     var->key_block = kb == 0 ? attn::kBN : kb;
   }

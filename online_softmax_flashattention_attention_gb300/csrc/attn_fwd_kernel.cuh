@@ -46,8 +46,9 @@
 namespace attn {
 
 constexpr int kBM = 128;           // query rows per tile (= tensor-memory lanes)
-constexpr int kBN = 128;           // keys per block (kBNWide: the d = 128 option of attn_fwd_ex)
+constexpr int kBN = 128;           // keys per block (kBNWide, kBNNarrow: d = 128 options of attn_fwd_ex)
 constexpr int kBNWide = 192;
+constexpr int kBNNarrow = 64;
 constexpr int kWarpTma = 4;
 constexpr int kWarpPv = 5;
 constexpr int kWarpS = 6;
@@ -105,11 +106,13 @@ __device__ __forceinline__ int fast_div(int n, uint32_t m, uint32_t s) {
 constexpr int kMaxSortedSeqs = 512;
 
 // BN: keys per block.  128 everywhere by default.  At d = 128 a forward with O out can take
-// 192-key blocks instead (attn_fwd_ex, key_block = 192): tensor memory then holds two score
-// buffers of 192 columns and o~ (512 columns), shared memory Q and two K/V stages of 48 KB.
-// Measured on GB300 it is slower (two score buffers leave the softmax warps waiting for
-// scores); it stays as an option because it is the same recurrence over other blocks, which
-// a test compares with the 128-key build.
+// 192- or 64-key blocks instead (attn_fwd_ex, key_block).  With 192, tensor memory holds two
+// score buffers of 192 columns and o~ (512 columns), shared memory Q and two K/V stages of
+// 48 KB; with 64, three score buffers of 64 columns and o~ (320 columns), Q and four K/V
+// stages of 16 KB.  Both are measured slower on GB300: 192 because two score buffers leave
+// the softmax warps waiting for scores, 64 because every block's hand-offs and rescale now
+// cover half the keys.  They stay as options because they are the same recurrence over other
+// blocks, which the tests compare with the 128-key build.
 template <int D, int BN = kBN>
 struct FwdCfg {
   static constexpr int kBNc = BN;
@@ -118,8 +121,8 @@ struct FwdCfg {
   static constexpr int kSubBytesKV = BN * 128;          // BN rows x 64 bf16
   static constexpr int kQBytes = kSub * kSubBytesQ;     // 128 rows x D bf16
   static constexpr int kKVBytes = kSub * kSubBytesKV;   // BN rows x D bf16
-  static constexpr int kStages = BN != kBN ? 2 : (D == 128) ? 3 : 4;  // K/V ring depth
-  static constexpr int kSBufs = BN != kBN ? 2 : 3;      // tensor-memory score buffers
+  static constexpr int kStages = BN > kBN ? 2 : (BN < kBN || D == 64) ? 4 : 3;  // K/V ring depth
+  static constexpr int kSBufs = BN > kBN ? 2 : 3;       // tensor-memory score buffers
   // How a tile's O leaves (measured on GB300): at d = 64 it is staged in the V stage of the
   // tile's last block and stored by TMA (a 16 KB tile in a 4-deep ring); at d = 128 the
   // stage would take a third of the ring while the store reads it, so each thread stores

@@ -124,24 +124,33 @@ def test_splitkv_workspace_checks(lib):
 
 
 def test_options_struct_checks(lib):
+    # The options are checked before the arguments.  Every call passes a Q that is not
+    # 16-byte aligned, so a call whose options are accepted stops at the alignment check
+    # (-4) and none of them reaches a GPU, on any machine.
     def call(**kw):
         o = pkg.AttnOptions(ctypes.sizeof(pkg.AttnOptions), kw.get("tau", 0.0), kw.get("mode", 0), kw.get("kb", 0))
         if "size" in kw:
             o.size = kw["size"]
-        return lib.attn_fwd_ex(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, 256, 256, 64, 0.125, 0, None,
-                               ctypes.byref(o), None)
+        return lib.attn_fwd_ex(0x10008, 0x20000, 0x30000, 0x40000, 0x50000, 1, 2, 256, 256, kw.get("d", 64), 0.125,
+                               0, None, ctypes.byref(o), None)
     assert call(size=4) == -8
     assert call(tau=-1.0) == -8
     assert call(tau=21.0) == -8
     assert call(tau=float("nan")) == -8
     assert call(mode=3) == -8
     assert call(mode=-1) == -8
-    assert call(kb=64) == -8                 # keys per block: 0, 128 or 192
-    assert call(kb=192, mode=2) == -8        # the 192-key build takes the hardware exponentials
-    # a struct that ends before key_block (its size was 16 bytes) is still accepted: the
-    # call gets past the options (and fails later only for want of a GPU here)
-    assert call(size=16) != -8
-    assert call(kb=192) != -8
+    assert call(kb=32) == -8                 # keys per block: 0, 64, 128 or 192
+    assert call(kb=256) == -8
+    assert call(kb=192, mode=2) == -8        # the 64- and 192-key builds take the hardware exponentials
+    assert call(kb=64, mode=2) == -8
+    # accepted options: the call gets past them to the alignment check.  A struct that
+    # ends before key_block (its size was 16 bytes) is accepted and gets the default.
+    assert call() == -4
+    assert call(size=16) == -4
+    assert call(kb=128) == -4
+    assert call(kb=192, d=128) == -4
+    assert call(kb=64, d=128) == -4
+    assert call(tau=20.0, mode=2) == -4
     assert ctypes.sizeof(pkg.AttnOptions) == 24
 
 

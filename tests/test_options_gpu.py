@@ -185,44 +185,50 @@ WIDE_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("kb", [64, 192])
 @pytest.mark.parametrize("shape", WIDE_SHAPES)
-def test_key_block_192_matches_128_and_oracle(shape):
+def test_key_block_matches_128_and_oracle(shape, kb):
     """The recurrence's result does not depend on the key-block size ("FlashAttention
     math", "Proof of exactness"; "Tiled attention: running max softmax" varies the tile):
-    the 192-key build agrees with the oracle and with the 128-key build within the
-    tolerance, with the pages' rescale rule and with the lazy option."""
+    the 64- and 192-key builds agree with the oracle and with the 128-key build within
+    the tolerance, with the pages' rescale rule and with the lazy option."""
     B, H, Nq, Nk, causal, lens = shape
     x = custom(B, H, Nq, Nk, 128, causal, seed=Nq + Nk + 5, lens=lens)
     O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"])
     for tau in (0.0, 5.5):
         O128, L128 = run_ex(x, tau, 1)
-        O192, L192 = run_ex(x, tau, 1, key_block=192)
-        compare(O192, L192, O_ref, LSE_ref)
-        compare(O192, L192, O128, L128)
+        Okb, Lkb = run_ex(x, tau, 1, key_block=kb)
+        compare(Okb, Lkb, O_ref, LSE_ref)
+        compare(Okb, Lkb, O128, L128)
 
 
-def test_key_block_192_full_size_every_item():
-    """B4 H16 N2048 d128 causal with 192-key blocks: two rows of every work item against the
-    oracle, and every row against the 128-key build."""
+@pytest.mark.parametrize("kb", [64, 192])
+def test_key_block_full_size_every_item(kb):
+    """B4 H16 N2048 d128 causal with 64- or 192-key blocks: two rows of every work item
+    against the oracle, and every row against the 128-key build."""
     x = gen.make_inputs("causal_b4h16n2048d128")
-    O192, L192 = run_ex(x, 0.0, 1, key_block=192)
+    Okb, Lkb = run_ex(x, 0.0, 1, key_block=kb)
     O128, L128 = run_ex(x, 0.0, 1)
-    compare(O192, L192, O128, L128)
+    compare(Okb, Lkb, O128, L128)
     rng = np.random.default_rng(12)
     picks = sorted({p for b in range(4) for h in range(16) for t0 in range(0, 2048, 128)
                     for p in ((b, h, int(rng.integers(t0, t0 + 128))), (b, h, t0 + 127))})
     O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], True, None, picks)
     idx = tuple(np.array(picks).T)
-    compare(O192[idx], L192[idx], O_ref, LSE_ref)
+    compare(Okb[idx], Lkb[idx], O_ref, LSE_ref)
 
 
-def test_key_block_192_rejected_where_not_built():
+@pytest.mark.parametrize("kb", [64, 192])
+def test_key_block_rejected_where_not_built(kb):
     pkg = _pkg()
     x = custom(1, 2, 256, 256, 64, False, seed=3)
     with pytest.raises(pkg.AttnError) as err:
-        run_ex(x, 0.0, 1, key_block=192)          # d = 64
+        run_ex(x, 0.0, 1, key_block=kb)           # d = 64
     assert err.value.status == -8
     x = custom(1, 2, 256, 256, 128, False, seed=4)
     with pytest.raises(pkg.AttnError) as err:
-        run_ex(x, 0.0, 2, key_block=192)          # mixed exponentials
+        run_ex(x, 0.0, 2, key_block=kb)           # mixed exponentials
+    assert err.value.status == -8
+    with pytest.raises(pkg.AttnError) as err:
+        run_ex(x, 0.0, 1, key_block=96)           # a size that is not built
     assert err.value.status == -8
