@@ -128,3 +128,93 @@ def test_random_packed_sequences_match_oracle(i, H, d, causal, lq, lk):
             O_ref[h], L_ref[h] = oracle.attention_head(oracle.bf16_to_f64(qs[b][h]), oracle.bf16_to_f64(ks[b][h]),
                                                        oracle.bf16_to_f64(vs[b][h]), scale, causal)
         compare(Of[rows].transpose(1, 0, 2), Lf[:, rows], O_ref, L_ref)
+
+
+def _draw_layouts(n: int):
+    """Strided problems: every tensor stored [B, N, H', d'] with H' >= H heads and d' >= d
+    columns per row (gaps between heads and between rows), viewed as [B, H, N, d]."""
+    rng = np.random.default_rng(SEED + 2)
+    cases = []
+    for i in range(n):
+        d = int(rng.choice([64, 128]))
+        B, H = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+        Nq, Nk = int(rng.integers(1, 600)), int(rng.integers(1, 800))
+        causal = bool(rng.random() < 0.5)
+        lens = [int(v) for v in rng.integers(0, Nk + 1, size=B)] if rng.random() < 0.3 else None
+        extra_h = int(rng.integers(0, 3))                     # unused heads between the used ones
+        extra_d = int(rng.choice([0, 8, 64]))                 # unused columns after each row
+        cases.append((i, B, H, Nq, Nk, d, causal, lens, extra_h, extra_d))
+    return cases
+
+
+LAYOUT_CASES = _draw_layouts(12)
+
+
+def _strided(codes, extra_h, extra_d, fill):
+    """[B, H, N, d] codes placed in a [B, N, H + extra_h, d + extra_d] tensor, returned as
+    the [B, H, N, d] view and the whole storage."""
+    import torch
+    B, H, N, d = codes.shape
+    big = torch.full((B, N, H + extra_h, d + extra_d), fill, dtype=torch.bfloat16, device="cuda")
+    view = big[:, :, :H, :d].transpose(1, 2)
+    view.copy_(to_device(codes))
+    return view, big
+
+
+@pytest.mark.parametrize("i,B,H,Nq,Nk,d,causal,lens,extra_h,extra_d", LAYOUT_CASES,
+                         ids=[f"s{c[0]}" for c in LAYOUT_CASES])
+def test_random_strided_layouts_match_oracle(i, B, H, Nq, Nk, d, causal, lens, extra_h, extra_d):
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    w = dict(name="fuzz_strided", B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=causal, qk=("normal", 0.0, 1.0),
+             v=("normal", 0.0, 1.0), seed=SEED + 303 * i, lens=None if lens is None else ("given", lens),
+             plant=None, scale=1.0 / math.sqrt(d))
+    x = gen.make_inputs(w)
+    Q, _ = _strided(x["Q"], extra_h, extra_d, 0.0)
+    K, _ = _strided(x["K"], extra_h, extra_d, 0.0)
+    V, _ = _strided(x["V"], extra_h, extra_d, 0.0)
+    O, Obig = _strided(np.zeros((B, H, Nq, d), np.uint16), extra_h, extra_d, 7.0)
+    LSE = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    lt = None if lens is None else torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    pkg.attn_fwd_strided(Q, K, V, O, LSE, scale=x["scale"], causal=causal, key_padding_lens=lt)
+    pkg.status_sync()
+    if extra_d:
+        assert torch.all(Obig[..., d:] == 7.0), "the gap after a row of O was written"
+    if extra_h:
+        assert torch.all(Obig[:, :, H:, :] == 7.0), "an unused head of O was written"
+    O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"])
+    compare(O.float().cpu().numpy().astype(np.float64), LSE.cpu().numpy().astype(np.float64), O_ref, LSE_ref)
+
+
+def _draw_splitkv(n: int):
+    """Few query rows against long key ranges, the shapes split-KV is for."""
+    rng = np.random.default_rng(SEED + 3)
+    cases = []
+    for i in range(n):
+        d = int(rng.choice([64, 128]))
+        B, H = int(rng.integers(1, 3)), int(rng.integers(1, 5))
+        Nq, Nk = int(rng.integers(1, 300)), int(rng.integers(200, 5000))
+        causal = bool(rng.random() < 0.5)
+        lens = [int(v) for v in rng.integers(0, Nk + 1, size=B)] if rng.random() < 0.4 else None
+        splits = int(rng.choice([0, 2, 3, 5, 8]))            # 0: the library chooses
+        cases.append((i, B, H, Nq, Nk, d, causal, lens, splits))
+    return cases
+
+
+SPLITKV_FUZZ = _draw_splitkv(10)
+
+
+@pytest.mark.parametrize("i,B,H,Nq,Nk,d,causal,lens,splits", SPLITKV_FUZZ, ids=[f"k{c[0]}" for c in SPLITKV_FUZZ])
+def test_random_splitkv_matches_oracle(i, B, H, Nq, Nk, d, causal, lens, splits):
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    w = dict(name="fuzz_splitkv", B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=causal, qk=("normal", 0.0, 1.0),
+             v=("normal", 0.0, 1.0), seed=SEED + 505 * i, lens=None if lens is None else ("given", lens),
+             plant=None, scale=1.0 / math.sqrt(d))
+    x = gen.make_inputs(w)
+    lt = None if lens is None else torch.as_tensor(np.asarray(lens, np.int32)).cuda()
+    O, LSE = pkg.attn_fwd_splitkv(to_device(x["Q"]), to_device(x["K"]), to_device(x["V"]), num_splits=splits,
+                                  scale=x["scale"], causal=causal, key_padding_lens=lt)
+    pkg.status_sync()
+    O_ref, LSE_ref = oracle.attention(x["Q"], x["K"], x["V"], x["scale"], causal, x["lens"])
+    compare(O.float().cpu().numpy().astype(np.float64), LSE.cpu().numpy().astype(np.float64), O_ref, LSE_ref)
