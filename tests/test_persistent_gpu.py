@@ -148,3 +148,36 @@ def test_tens_of_thousands_of_heads_every_item(B, H, N, d, causal, lens_kind):
     idx = tuple(np.array(picks).T)
     compare(O[idx], LSE[idx], O_ref, LSE_ref)
     assert np.all(np.isfinite(O))
+
+
+@pytest.mark.parametrize("B,H,d,causal", [
+    (2, 70000, 128, True),      # one-tile kernel: 2.29e9 elements per tensor
+    (2, 140000, 64, False),     # two-tile kernel: 2.29e9 elements per tensor
+])
+def test_tensors_beyond_two_to_the_31_elements(B, H, d, causal):
+    """Q, K, V and O each hold more than 2^31 elements (4.6 GB of bf16 each), so the rows of
+    the last heads lie past every 32-bit element offset: O's row addresses, the LSE index
+    and the tensor maps' head coordinates must all be computed in 64 bits.  Rows of heads
+    on both sides of element 2^31 are compared with the oracle; only those rows are copied
+    back."""
+    import torch
+    import online_softmax_flashattention_attention_gb300 as pkg
+    N = 128
+    assert B * H * N * d > 2 ** 31
+    x = custom(B, H, N, N, d, causal, seed=47 + d)
+    Q, K, V = to_device(x["Q"]), to_device(x["K"]), to_device(x["V"])
+    O = torch.full_like(Q, float("nan"))
+    LSE = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    pkg.attn_fwd(Q, K, V, O, LSE, scale=x["scale"], causal=causal)
+    pkg.status_sync()
+    first_past = (2 ** 31) // (N * d)                 # the first (b, h) whose rows start past 2^31
+    bh_picks = sorted({0, H - 1, H, first_past - 1, first_past, first_past + 1, B * H - 2, B * H - 1})
+    rng = np.random.default_rng(d)
+    bh_picks += [int(v) for v in rng.integers(first_past, B * H, size=6)]
+    picks = sorted({(bh // H, bh % H, i) for bh in bh_picks for i in (0, 1, 63, 64, 126, 127)})
+    idx = tuple(torch.as_tensor(np.array(picks).T, device="cuda"))
+    Os = O[idx].float().cpu().numpy().astype(np.float64)
+    Ls = LSE[idx].cpu().numpy().astype(np.float64)
+    O_ref, LSE_ref = oracle.attention_rows(x["Q"], x["K"], x["V"], x["scale"], causal, None, picks)
+    compare(Os, Ls, O_ref, LSE_ref)
+    assert not torch.isnan(O).any().item() and not torch.isnan(LSE).any().item(), "a row was left unwritten"
