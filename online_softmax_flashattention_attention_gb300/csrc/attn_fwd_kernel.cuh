@@ -121,7 +121,10 @@ struct FwdCfg {
   static constexpr int kSubBytesKV = BN * 128;          // BN rows x 64 bf16
   static constexpr int kQBytes = kSub * kSubBytesQ;     // 128 rows x D bf16
   static constexpr int kKVBytes = kSub * kSubBytesKV;   // BN rows x D bf16
-  static constexpr int kStages = BN > kBN ? 2 : (BN < kBN || D == 64) ? 4 : 3;  // K/V ring depth
+  // K/V ring depth.  At d = 128 with 128-key blocks, three stages each are all that fit beside
+  // Q; measured on GB300, two stages each are 11-18 % slower, and two K with four V stages
+  // run the same as three and three.
+  static constexpr int kStages = BN > kBN ? 2 : (BN < kBN || D == 64) ? 4 : 3;
   static constexpr int kSBufs = BN > kBN ? 2 : 3;       // tensor-memory score buffers
   // How a tile's O leaves (measured on GB300): at d = 64 it is staged in the V stage of the
   // tile's last block and stored by TMA (a 16 KB tile in a 4-deep ring); at d = 128 the
